@@ -1,0 +1,19 @@
+"""Float64 CPU oracle for the flash-CCE ORPO head.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this package:
+only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg may call it.  It shares no code with the CUDA library under
+``orpo_preference_loss_gb300/``.
+"""
+
+from .orpo_oracle import (  # noqa: F401
+    bf16_bits_to_f64,
+    log1mexp,
+    softcap_value,
+    softcap_slope,
+    head_forward,
+    orpo_loss,
+    head_backward,
+    full_chain,
+    OracleError,
+)

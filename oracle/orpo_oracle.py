@@ -1,0 +1,277 @@
+"""Plain float64 oracle for the flash-CCE ORPO head (CPU, numpy).
+
+TEST INFRASTRUCTURE ONLY: tests, the smoke check and the benchmark's CPU
+baseline call this module; the CUDA library never does.  Every quantity is the
+plain definition written out in float64 on the exact values of the bf16 inputs
+(no rounding to bf16 or fp32 anywhere), with the vocabulary processed in row
+chunks so that a bounded ``[chunk, V]`` block is the largest array held.
+
+Sources (mlx-bun "Training — design (ORPO, flash-CCE head, prefix sharing,
+segmented backward)" page, and the "Steel flash-CCE — handoff" page):
+
+* ``head_forward``  — §5.1 "The head: from token-chunking to the flash-CCE
+  kernel": per-token ``logp_t = z~[t, y_t] - logsumexp_v z~[t, v]`` with
+  ``z = h W^T`` and the Gemma final-logit softcap ``z~ = c tanh(z / c)``
+  (implementation spec of the fused linear-CE head, forward bullet).
+* ``orpo_loss``     — §1 "The objective": ``L = NLL(chosen) + lambda * L_OR``,
+  ``L_OR = -log sigmoid(log_odds)``,
+  ``log_odds = (l_w - l_r) - (log1mexp(l_w) - log1mexp(l_r))`` with ``l`` the
+  length-normalised (mean) response log-probability; batch reduction
+  ``nll = mean(-l_w)``, ``or = mean(softplus(-log_odds))`` (file-by-file
+  ``loss.ts`` bullet); metrics loss / nll / or / accuracy (``l_w > l_r``) /
+  margin (mean chosen-minus-rejected log-odds, "Small sets over-fit fast").
+  NLL scope is the ``response`` reading (``NLL = -l_w``).
+* ``head_backward`` — implementation spec, backward bullet: recompute the
+  logits, ``dZ = g * (onehot_y - softmax(z~)) * sech^2(z / c)``, then
+  ``dh = dZ W`` and (the head-weight gradient that the pages leave to the
+  head-LoRA follow-on) ``dW = dZ^T h``.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, library routines, invariants and central finite differences).
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+LN2 = math.log(2.0)
+
+
+class OracleError(ValueError):
+    """Raised where the GPU library reports a data error through its status word."""
+
+    def __init__(self, kind: str, msg: str):
+        super().__init__(f"{kind}: {msg}")
+        self.kind = kind
+
+
+# --------------------------------------------------------------------------
+# inputs
+# --------------------------------------------------------------------------
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact float64 value of bf16 bit patterns (uint16): bf16 is the top half of fp32."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    f32 = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return f32.astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# scalar pieces
+# --------------------------------------------------------------------------
+
+def log1mexp(x):
+    """log(1 - exp(x)) for x < 0, two-branch form (Maechler 2012).
+
+    The ORPO objective (§1) needs log(1 - e^l) for the mean log-prob l; the pages
+    flag the x -> 0^- end as the NaN hazard and ask for a clamp or a two-branch
+    form.  Branch point -ln 2: log(-expm1(x)) above it, log1p(-exp(x)) below.
+    x = 0 gives -inf (the GPU path reports that as a non-finite loss).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(divide="ignore"):
+        out = np.where(x > -LN2,
+                       np.log(-np.expm1(np.minimum(x, 0.0))),
+                       np.log1p(-np.exp(np.minimum(x, 0.0))))
+    if np.any(x > 0):
+        raise OracleError("arg", "log1mexp is defined for x <= 0 only")
+    return out if out.ndim else float(out)
+
+
+def softplus(x):
+    x = np.asarray(x, dtype=np.float64)
+    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def sigmoid(x):
+    x = np.asarray(x, dtype=np.float64)
+    e = np.exp(-np.abs(x))
+    return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def softcap_value(z: np.ndarray, c: float) -> np.ndarray:
+    """z~ = c * tanh(z / c) when c > 0, else z (softcap off)."""
+    return c * np.tanh(z / c) if c > 0 else z
+
+
+def softcap_slope(z: np.ndarray, c: float) -> np.ndarray:
+    """d z~ / d z = 1 - tanh^2(z / c) = sech^2(z / c) when c > 0, else 1."""
+    if c > 0:
+        t = np.tanh(z / c)
+        return 1.0 - t * t
+    return np.ones_like(z)
+
+
+def _row_chunk(V: int, budget_elems: int = 1 << 23) -> int:
+    return max(1, budget_elems // max(1, V))
+
+
+# --------------------------------------------------------------------------
+# head forward: logp and lse
+# --------------------------------------------------------------------------
+
+def head_forward(h: np.ndarray, W: np.ndarray, targets: np.ndarray, mask: np.ndarray,
+                 softcap: float = 0.0):
+    """Per-token response log-prob and log-sum-exp.
+
+    h [M, d], W [V, d] float64; targets [M] int; mask [M] (0 = prompt/pad row).
+    Returns (logp [M], lse [M]).  lse is defined for every row; logp is 0 on
+    mask = 0 rows, whose targets are never read.  A target outside [0, V) on a
+    mask = 1 row raises OracleError("target").
+    """
+    h = np.asarray(h, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    M, V = h.shape[0], W.shape[0]
+    targets = np.asarray(targets).astype(np.int64)
+    mask = np.asarray(mask).astype(bool)
+    logp = np.zeros(M, dtype=np.float64)
+    lse = np.zeros(M, dtype=np.float64)
+    bad = mask & ((targets < 0) | (targets >= V))
+    if np.any(bad):
+        raise OracleError("target", f"target out of range on row {int(np.argmax(bad))}")
+    step = _row_chunk(V)
+    for r0 in range(0, M, step):
+        r1 = min(M, r0 + step)
+        z = softcap_value(h[r0:r1] @ W.T, softcap)          # [rows, V]
+        zmax = z.max(axis=1)
+        lse[r0:r1] = zmax + np.log(np.exp(z - zmax[:, None]).sum(axis=1))
+        rows = np.arange(r1 - r0)
+        m = mask[r0:r1]
+        tgt = z[rows[m], targets[r0:r1][m]]
+        logp[r0:r1][m] = tgt - lse[r0:r1][m]
+    return logp, lse
+
+
+# --------------------------------------------------------------------------
+# ORPO loss over sequences / pairs
+# --------------------------------------------------------------------------
+
+@dataclass
+class LossResult:
+    loss: float
+    nll: float
+    orr: float          # mean L_OR
+    accuracy: float
+    margin: float
+    ell: np.ndarray     # [2P] mean response log-prob per sequence
+    log_odds: np.ndarray  # [P]
+    g: np.ndarray       # [M] dL/dlogp_t
+    n: np.ndarray       # [2P] response-token count per sequence
+
+    def metrics(self) -> np.ndarray:
+        return np.array([self.loss, self.nll, self.orr, self.accuracy, self.margin])
+
+
+def orpo_loss(logp: np.ndarray, seq_id: np.ndarray, mask: np.ndarray, n_pairs: int,
+              lam: float) -> LossResult:
+    """ORPO objective and its gradient with respect to every per-token logp.
+
+    Sequence 2p is the chosen response of pair p and 2p+1 the rejected one.
+    Rows with seq_id = -1 are padding.  l_s is the mean of logp over the
+    mask = 1 rows of sequence s.  Per pair:
+        x_p  = (l_w - l_r) - (log1mexp(l_w) - log1mexp(l_r))
+        L    = (1/P) sum_p [ -l_w + lam * softplus(-x_p) ]
+    Gradient (closed form; d x / d l_w = 1 / (1 - e^{l_w})):
+        G_w = (1/P) (-1 - lam * sigmoid(-x) / (1 - e^{l_w}))
+        G_r = (1/P) ( lam * sigmoid(-x) / (1 - e^{l_r}))
+        g_t = mask_t * G_{s(t)} / n_{s(t)}
+    """
+    logp = np.asarray(logp, dtype=np.float64)
+    seq_id = np.asarray(seq_id).astype(np.int64)
+    mask = np.asarray(mask).astype(bool)
+    P = int(n_pairs)
+    if P < 1:
+        raise OracleError("arg", "n_pairs must be >= 1")
+    S = 2 * P
+    if np.any((seq_id < -1) | (seq_id >= S)):
+        raise OracleError("seqid", "sequence id out of range")
+    valid = seq_id >= 0
+    ids = seq_id[valid]
+    if np.any(np.diff(ids) < 0):
+        raise OracleError("seqid", "sequence ids are not non-decreasing")
+    use = valid & mask
+    n = np.bincount(seq_id[use], minlength=S).astype(np.float64)
+    if np.any(n == 0):
+        raise OracleError("empty", f"sequence {int(np.argmin(n))} has no response token")
+    tot = np.bincount(seq_id[use], weights=logp[use], minlength=S)
+    ell = tot / n
+    lw, lr = ell[0::2], ell[1::2]
+    if np.any(ell > 0):
+        raise OracleError("nonfinite", "a mean log-prob is positive")
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        x = (lw - lr) - (log1mexp(lw) - log1mexp(lr))
+        lor = softplus(-x)
+        nll = float(np.mean(-lw))
+        orr = float(np.mean(lor))
+        loss = nll + lam * orr
+        acc = float(np.mean(lw > lr))
+        margin = float(np.mean(x))
+        sig = sigmoid(-x)
+        # 1 / (1 - e^l) = -1 / expm1(l)
+        inv_w = -1.0 / np.expm1(lw)
+        inv_r = -1.0 / np.expm1(lr)
+        Gw = (-1.0 - lam * sig * inv_w) / P
+        Gr = (lam * sig * inv_r) / P
+    # l = 0 (a response whose every target has probability 1) makes log1mexp
+    # -inf; the value and gradient are then reported as non-finite, not clamped.
+    if not (np.isfinite(loss) and np.all(np.isfinite(x)) and np.all(np.isfinite(Gw))
+            and np.all(np.isfinite(Gr))):
+        raise OracleError("nonfinite", "loss, log-odds or gradient is not finite")
+    G = np.empty(S)
+    G[0::2], G[1::2] = Gw, Gr
+    g = np.zeros_like(logp)
+    g[use] = G[seq_id[use]] / n[seq_id[use]]
+    return LossResult(loss=loss, nll=nll, orr=orr, accuracy=acc, margin=margin,
+                      ell=ell, log_odds=x, g=g, n=n)
+
+
+# --------------------------------------------------------------------------
+# head backward: dh and dW
+# --------------------------------------------------------------------------
+
+def head_backward(h: np.ndarray, W: np.ndarray, targets: np.ndarray, mask: np.ndarray,
+                  lse: np.ndarray, g: np.ndarray, softcap: float = 0.0):
+    """dh = dZ W and dW = dZ^T h with dZ = g (onehot_y - softmax(z~)) sech^2(z/c).
+
+    softmax is rebuilt from the given lse: p = exp(z~ - lse).  Rows with
+    mask = 0 carry no gradient (their g is treated as 0 and their target is not
+    read).  Returns (dh [M, d], dW [V, d]) in float64.
+    """
+    h = np.asarray(h, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    M, d = h.shape
+    V = W.shape[0]
+    targets = np.asarray(targets).astype(np.int64)
+    mask = np.asarray(mask).astype(bool)
+    lse = np.asarray(lse, dtype=np.float64)
+    g = np.where(mask, np.asarray(g, dtype=np.float64), 0.0)
+    dh = np.zeros((M, d))
+    dW = np.zeros((V, d))
+    step = _row_chunk(V)
+    for r0 in range(0, M, step):
+        r1 = min(M, r0 + step)
+        gr = g[r0:r1]
+        if not np.any(gr != 0.0):
+            continue
+        z = h[r0:r1] @ W.T
+        zt = softcap_value(z, softcap)
+        p = np.exp(zt - lse[r0:r1, None])
+        onehot = np.zeros_like(p)
+        rows = np.arange(r1 - r0)
+        m = mask[r0:r1]
+        onehot[rows[m], targets[r0:r1][m]] = 1.0
+        dZ = gr[:, None] * (onehot - p) * softcap_slope(z, softcap)
+        dh[r0:r1] = dZ @ W
+        dW += dZ.T @ h[r0:r1]
+    return dh, dW
+
+
+def full_chain(h, W, targets, mask, seq_id, n_pairs, lam, softcap=0.0):
+    """Forward, loss and backward in sequence, as one training step of the head."""
+    logp, lse = head_forward(h, W, targets, mask, softcap)
+    res = orpo_loss(logp, seq_id, mask, n_pairs, lam)
+    dh, dW = head_backward(h, W, targets, mask, lse, res.g, softcap)
+    return logp, lse, res, dh, dW
