@@ -1,0 +1,167 @@
+/*
+ * orpo_head.h — C ABI of the flash-CCE ORPO head for one GB300 GPU (sm_103a).
+ *
+ * The head computes, for M response rows of hidden state h and a vocabulary
+ * head W, the per-token log-probability of the target token, the ORPO loss
+ * over chosen / rejected pairs, and the gradients of that loss with respect to
+ * h and W, without ever holding the [M, V] logits in memory.
+ *
+ * Where each operation is defined (mlx-bun documentation pages):
+ *   - "Training — design (ORPO, flash-CCE head, prefix sharing, segmented
+ *     backward)", §1 "The objective" (ORPO loss, log1mexp log-odds, mean
+ *     response log-prob), §5.1 "The head: from token-chunking to the flash-CCE
+ *     kernel" (tier 4: vocab-parallel online softmax, per-block partials and
+ *     their merge, recompute backward), and the fused linear-CE implementation
+ *     spec (forward / backward bullets, Gemma softcap and its sech^2 slope);
+ *   - "Steel flash-CCE — handoff", "The architecture (what's proven)"
+ *     (forward partials per vocab block, backward coefficient
+ *     g * (onehot - softmax(logit - lse)) * sech^2 and its contraction into dh).
+ * The weight gradient dW = dZ^T h is the head-LoRA follow-on that the design
+ * page leaves open; it is computed here with the same dZ.
+ *
+ * Conventions shared by every entry point
+ *   - Layouts are row-major and contiguous: h [M, d] bf16, W [V, d] bf16,
+ *     dh [M, d] fp32, dW [V, d] fp32; per-row vectors have M entries.
+ *   - bf16 data is passed as raw 16-bit words (uint16 bit patterns).
+ *   - Every pointer argument is a DEVICE pointer except the stream handle.
+ *     The caller allocates every buffer, including the workspace, and keeps
+ *     them alive until the work on `stream` has finished.  The library never
+ *     allocates, frees or caches device memory and keeps no pointer after it
+ *     returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is asynchronous and stream-ordered.
+ *   - Return value: ORPO_OK or a host-detected error code (< 16).  On an error
+ *     nothing is launched and no output is touched.
+ *   - `status` (device int32, 1 word): data errors found on the GPU are OR-ed
+ *     into it as ORPO_STATUS_* bits.  The caller zeroes it before the first
+ *     call and reads it after synchronising.  Device code never traps.
+ *   - Alignment: h, W, dh, dW and the workspace must be 16-byte aligned
+ *     (cudaMalloc'd memory is 256-byte aligned); d must be a multiple of 8.
+ *   - Requires a compute-capability 10.3 device (GB300); other devices get
+ *     ORPO_ERR_UNSUPPORTED.
+ */
+#ifndef ORPO_HEAD_H
+#define ORPO_HEAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* host-detected return codes */
+enum {
+  ORPO_OK = 0,
+  ORPO_ERR_NULL = 1,        /* a required pointer is NULL */
+  ORPO_ERR_SHAPE = 2,       /* M, V, d or n_pairs out of the supported range */
+  ORPO_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned or d % 8 != 0 */
+  ORPO_ERR_ARG = 4,         /* softcap / lambda not finite, or lambda < 0 */
+  ORPO_ERR_WORKSPACE = 5,   /* ws_bytes < orpo_head_workspace_bytes(M, V, d) */
+  ORPO_ERR_CUDA = 6,        /* a CUDA runtime call or a launch failed */
+  ORPO_ERR_UNSUPPORTED = 7  /* the current device is not compute capability 10.3 */
+};
+
+/* device-detected status bits (OR-ed into *status) */
+enum {
+  ORPO_STATUS_TARGET = 1 << 4,     /* a mask = 1 row has a target outside [0, V) */
+  ORPO_STATUS_SEQID = 1 << 5,      /* seq_id outside [-1, 2P) or ids not non-decreasing */
+  ORPO_STATUS_EMPTY_SEQ = 1 << 6,  /* a sequence has no mask = 1 row (its mean is undefined) */
+  ORPO_STATUS_NONFINITE = 1 << 7,  /* a non-finite lse, loss, log-odds or gradient */
+  ORPO_STATUS_TIMEOUT = 1 << 8     /* a bounded on-chip wait gave up (the kernel returned early) */
+};
+
+/* Largest number of pairs orpo_loss accepts. */
+#define ORPO_MAX_PAIRS 2048
+
+/*
+ * Bytes of scratch that orpo_head_fwd and orpo_head_bwd need for these sizes
+ * (one workspace serves both).  It holds the per-vocab-split partials of the
+ * forward (O(M)) and the bounded bf16 block of logit gradients that the
+ * backward streams through (at most 256 MiB whatever M and V are), so the
+ * extra memory never grows like M * V.  Returns 0 for invalid sizes.
+ */
+size_t orpo_head_workspace_bytes(int64_t M, int64_t V, int64_t d);
+
+/*
+ * Forward of the head (design page §5.1 tier 4; fused-head spec, forward).
+ *   z = h W^T (fp32 accumulation of bf16 products);
+ *   z~ = softcap * tanh(z / softcap) if softcap > 0, else z;
+ *   lse[t]  = log sum_v exp(z~[t, v])              for every row t;
+ *   logp[t] = z~[t, targets[t]] - lse[t]           for mask[t] = 1 rows,
+ *   logp[t] = 0                                    for mask[t] = 0 rows
+ *             (their targets are never read).
+ * The vocabulary is processed in splits with an online (max, sum-exp) state
+ * per row and merged per row at the end; no [M, V] buffer exists.
+ * targets: int32 [M]; mask: uint8 [M] (nonzero = response row).
+ * Device errors: ORPO_STATUS_TARGET (logp[t] is then 0),
+ * ORPO_STATUS_NONFINITE (an lse that is not finite).
+ * M = 0 is a no-op.  Limits: 1 <= V < 2^31, 8 <= d < 2^20, M < 2^31.
+ */
+int orpo_head_fwd(const void* h_bf16, const void* W_bf16, const int32_t* targets,
+                  const uint8_t* mask, int64_t M, int64_t V, int64_t d, float softcap,
+                  float* logp, float* lse, void* workspace, size_t ws_bytes,
+                  int32_t* status, void* stream);
+
+/*
+ * ORPO loss and its gradient with respect to every logp (design page §1;
+ * the length-normalised mean and the 1/(1 - P) gradient factor of §4).
+ * Sequence 2p is the chosen response of pair p, sequence 2p+1 the rejected one.
+ *   seq_id: int32 [M], -1 = padding row, else in [0, 2P); the ids that are not
+ *           -1 must be non-decreasing in row order (padding may sit anywhere).
+ *   l_s  = mean of logp over the mask = 1 rows of sequence s      -> ell[2P]
+ *   x_p  = (l_w - l_r) - (log1mexp(l_w) - log1mexp(l_r)), log1mexp(x) = log(1 - e^x)
+ *   loss = (1/P) sum_p [ -l_w + lambda * softplus(-x_p) ]  (NLL over the chosen response)
+ *   out[0..4] = loss, nll = mean(-l_w), or = mean(softplus(-x)),
+ *               accuracy = mean(l_w > l_r), margin = mean(x_p)
+ *   g[t] = dloss/dlogp[t] = mask[t] * G_{s(t)} / n_{s(t)}, with
+ *          G_w = (-1 - lambda * sigmoid(-x) / (1 - e^{l_w})) / P,
+ *          G_r = ( lambda * sigmoid(-x) / (1 - e^{l_r})) / P;  g = 0 on pad rows.
+ * Sums are taken in fp64 in a fixed order (bitwise reproducible).
+ * Device errors: ORPO_STATUS_SEQID, ORPO_STATUS_EMPTY_SEQ, ORPO_STATUS_NONFINITE
+ * (e.g. l = 0 makes log1mexp -inf; it is reported, not clamped).
+ * Limits: 1 <= n_pairs <= ORPO_MAX_PAIRS, 0 <= M < 2^31, lambda >= 0.
+ */
+int orpo_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int64_t M,
+              int32_t n_pairs, float lambda, float* out, float* ell, float* g,
+              int32_t* status, void* stream);
+
+/*
+ * Backward of the head (fused-head spec, backward bullet; steel handoff,
+ * backward structure).  With p = exp(z~ - lse) rebuilt from the saved lse and
+ * the logits recomputed tile by tile:
+ *   dZ[t, v] = g[t] * (onehot(v == targets[t]) - p[t, v]) * sech^2(z[t, v] / softcap)
+ *              (sech^2 factor only when softcap > 0; dZ = 0 on mask = 0 rows),
+ *   dh  = dZ W     (fp32 [M, d], overwritten),
+ *   dW  = dZ^T h   (fp32 [V, d]; overwritten, or added to when accumulate_dW != 0).
+ * g is dloss/dlogp (what orpo_loss returns).  dZ is rounded to bf16 once, in a
+ * bounded workspace block, before the two contractions; accumulation is fp32
+ * and the result does not depend on run-to-run scheduling (no float atomics).
+ * Device errors: ORPO_STATUS_TARGET.
+ */
+int orpo_head_bwd(const void* h_bf16, const void* W_bf16, const int32_t* targets,
+                  const uint8_t* mask, const float* lse, const float* g, int64_t M,
+                  int64_t V, int64_t d, float softcap, float* dh, float* dW,
+                  int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* status,
+                  void* stream);
+
+/* Text of a return code or of a set of ORPO_STATUS_* bits (static storage). */
+const char* orpo_status_string(int code);
+
+/*
+ * Diagnostic: C = A * B on the same tensor-core engine as the head, for
+ * checking the engine in isolation (a plain matrix product; it has no
+ * counterpart on the pages).  A is [M, K] bf16 row-major (a_mn_major = 0) or
+ * stored transposed as [K, M] (a_mn_major = 1); B is [N, K] (b_mn_major = 0)
+ * or stored as [K, N] (b_mn_major = 1); C is fp32 [M, N] row-major and is
+ * overwritten.  M, N, K >= 1; the contiguous extent of every operand must be a
+ * multiple of 8 elements and of C a multiple of 4.
+ */
+int orpo_debug_gemm(const void* A_bf16, const void* B_bf16, float* C, int64_t M, int64_t N,
+                    int64_t K, int a_mn_major, int b_mn_major, int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ORPO_HEAD_H */

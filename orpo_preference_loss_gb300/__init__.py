@@ -1,0 +1,187 @@
+"""GB300 (sm_103a) flash-CCE ORPO head: Python binding of liborpo_head.
+
+The functions here carry the C entry points' names and only marshal arguments:
+every step of the head runs in the library's CUDA kernels.  PyTorch supplies
+device memory and the current CUDA stream.  If the library has not been built
+(``python -c "import __graft_entry__ as g; g.build()"``) the calls raise; there
+is no fallback implementation.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "OrpoError", "load", "lib_path", "orpo_head_workspace_bytes", "orpo_head_fwd", "orpo_loss",
+    "orpo_head_bwd", "orpo_status_string", "orpo_debug_gemm", "OrpoHead", "STATUS_BITS",
+]
+
+STATUS_BITS = {"target": 1 << 4, "seqid": 1 << 5, "empty": 1 << 6, "nonfinite": 1 << 7, "timeout": 1 << 8}
+MAX_PAIRS = 2048
+
+_lib = None
+
+
+class OrpoError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {orpo_status_string(code)} (code {code})")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load liborpo_head.so (built in-tree); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with orpo_preference_loss_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    L.orpo_head_workspace_bytes.argtypes = [i64, i64, i64]
+    L.orpo_head_workspace_bytes.restype = sz
+    L.orpo_head_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp, vp, vp, sz, vp, vp]
+    L.orpo_head_fwd.restype = ctypes.c_int
+    L.orpo_loss.argtypes = [vp, vp, vp, i64, i32, f32, vp, vp, vp, vp, vp]
+    L.orpo_loss.restype = ctypes.c_int
+    L.orpo_head_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, vp, vp, ctypes.c_int, vp, sz, vp, vp]
+    L.orpo_head_bwd.restype = ctypes.c_int
+    L.orpo_status_string.argtypes = [ctypes.c_int]
+    L.orpo_status_string.restype = ctypes.c_char_p
+    L.orpo_debug_gemm.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, vp]
+    L.orpo_debug_gemm.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code, what):
+    if code != 0:
+        raise OrpoError(code, what)
+
+
+def _dev(t, name, dtypes, shape=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+BF16 = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (torch.bfloat16, torch.int16)
+
+
+def orpo_status_string(code: int) -> str:
+    return load().orpo_status_string(int(code)).decode()
+
+
+def orpo_head_workspace_bytes(M: int, V: int, d: int) -> int:
+    return int(load().orpo_head_workspace_bytes(M, V, d))
+
+
+def orpo_head_fwd(h, W, targets, mask, softcap, logp, lse, workspace, status, stream=None):
+    M, d = h.shape
+    V = W.shape[0]
+    _dev(h, "h", BF16)
+    _dev(W, "W", BF16, (V, d))
+    _dev(targets, "targets", (torch.int32,), (M,))
+    _dev(mask, "mask", (torch.uint8, torch.bool), (M,))
+    _dev(logp, "logp", (torch.float32,), (M,))
+    _dev(lse, "lse", (torch.float32,), (M,))
+    _dev(workspace, "workspace", (torch.uint8,))
+    _dev(status, "status", (torch.int32,))
+    _check(load().orpo_head_fwd(_ptr(h), _ptr(W), _ptr(targets), _ptr(mask), M, V, d, float(softcap),
+                                _ptr(logp), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(status),
+                                _stream(stream)), "orpo_head_fwd")
+
+
+def orpo_loss(logp, seq_id, mask, n_pairs, lam, out, ell, g, status, stream=None):
+    M = logp.shape[0]
+    _dev(logp, "logp", (torch.float32,), (M,))
+    _dev(seq_id, "seq_id", (torch.int32,), (M,))
+    _dev(mask, "mask", (torch.uint8, torch.bool), (M,))
+    _dev(out, "out", (torch.float32,), (5,))
+    _dev(ell, "ell", (torch.float32,), (2 * n_pairs,))
+    _dev(g, "g", (torch.float32,), (M,))
+    _dev(status, "status", (torch.int32,))
+    _check(load().orpo_loss(_ptr(logp), _ptr(seq_id), _ptr(mask), M, int(n_pairs), float(lam), _ptr(out),
+                            _ptr(ell), _ptr(g), _ptr(status), _stream(stream)), "orpo_loss")
+
+
+def orpo_head_bwd(h, W, targets, mask, lse, g, softcap, dh, dW, accumulate_dW, workspace, status,
+                  stream=None):
+    M, d = h.shape
+    V = W.shape[0]
+    _dev(h, "h", BF16)
+    _dev(W, "W", BF16, (V, d))
+    _dev(targets, "targets", (torch.int32,), (M,))
+    _dev(mask, "mask", (torch.uint8, torch.bool), (M,))
+    _dev(lse, "lse", (torch.float32,), (M,))
+    _dev(g, "g", (torch.float32,), (M,))
+    _dev(dh, "dh", (torch.float32,), (M, d))
+    _dev(dW, "dW", (torch.float32,), (V, d))
+    _dev(workspace, "workspace", (torch.uint8,))
+    _dev(status, "status", (torch.int32,))
+    _check(load().orpo_head_bwd(_ptr(h), _ptr(W), _ptr(targets), _ptr(mask), _ptr(lse), _ptr(g), M, V, d,
+                                float(softcap), _ptr(dh), _ptr(dW), 1 if accumulate_dW else 0, _ptr(workspace),
+                                workspace.numel(), _ptr(status), _stream(stream)), "orpo_head_bwd")
+
+
+def orpo_debug_gemm(A, B, C, M, N, K, a_mn_major, b_mn_major, status, stream=None):
+    _dev(A, "A", BF16)
+    _dev(B, "B", BF16)
+    _dev(C, "C", (torch.float32,), (M, N))
+    _check(load().orpo_debug_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(a_mn_major), int(b_mn_major),
+                                  _ptr(status), _stream(stream)), "orpo_debug_gemm")
+
+
+class OrpoHead:
+    """Owns the per-size device buffers (workspace, outputs) and runs one head step.
+
+    All tensors come from PyTorch's allocator; the step itself is the three C
+    entry points in order on the current stream.
+    """
+
+    def __init__(self, M: int, V: int, d: int, n_pairs: int, device="cuda"):
+        self.M, self.V, self.d, self.P = M, V, d, n_pairs
+        dev = torch.device(device)
+        self.workspace = torch.empty(orpo_head_workspace_bytes(M, V, d), dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.logp = torch.empty(M, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(M, dtype=torch.float32, device=dev)
+        self.out = torch.empty(5, dtype=torch.float32, device=dev)
+        self.ell = torch.empty(2 * n_pairs, dtype=torch.float32, device=dev)
+        self.g = torch.empty(M, dtype=torch.float32, device=dev)
+        self.dh = torch.empty((M, d), dtype=torch.float32, device=dev)
+        self.dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+
+    def step(self, h, W, targets, mask, seq_id, softcap, lam, accumulate_dW=False, stream=None):
+        orpo_head_fwd(h, W, targets, mask, softcap, self.logp, self.lse, self.workspace, self.status, stream)
+        orpo_loss(self.logp, seq_id, mask, self.P, lam, self.out, self.ell, self.g, self.status, stream)
+        orpo_head_bwd(h, W, targets, mask, self.lse, self.g, softcap, self.dh, self.dW, accumulate_dW,
+                      self.workspace, self.status, stream)
+        return self.out

@@ -1,0 +1,344 @@
+// api.cu — the C ABI of liborpo_head: argument checks, workspace layout, tensor
+// maps, blocking choices and the launch sequence of each entry point.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/orpo_head.h"
+#include "internal.h"
+
+namespace orpo {
+
+size_t loss_smem_bytes(int P);
+
+namespace {
+
+constexpr int64_t kMaxRows = (1ll << 31) - 1;
+
+// ---------------------------------------------------------------- driver entry point
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+// ---------------------------------------------------------------- device facts
+struct DevInfo {
+  int ok = -1;  // -1 unknown, 0 unsupported, 1 ok
+  int sms = 0;
+};
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+
+int device_check(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ORPO_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return ORPO_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& di = g_dev[dev];
+  if (di.ok < 0) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ORPO_ERR_CUDA;
+    di.ok = (major == 10 && minor == 3) ? 1 : 0;
+    di.sms = n;
+  }
+  if (!di.ok) return ORPO_ERR_UNSUPPORTED;
+  *sms = di.sms;
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode) return ORPO_ERR_CUDA;
+  return ORPO_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------- blocking
+struct BwdBlocks {
+  int64_t Mc, Vc;  // rows / columns of the scratch block (multiples of 128 / 256)
+};
+
+BwdBlocks bwd_blocks(int64_t M, int64_t V) {
+  const int64_t Mpad = std::max<int64_t>(kBM, cdiv(M, kBM) * kBM);
+  const int64_t Mc = std::min(Mpad, kMcMax);
+  const int64_t Vpad = cdiv(V, kBN) * kBN;
+  int64_t vc = (kScratchBudget / (2 * Mc)) / kBN * kBN;
+  vc = std::max<int64_t>(kBN, vc);
+  return BwdBlocks{Mc, std::min(Vpad, vc)};
+}
+
+size_t partial_bytes(int64_t M) {
+  const int64_t Mpad = std::max<int64_t>(kBM, cdiv(M, kBM) * kBM);
+  return (size_t)2 * kNsplitMax * Mpad * sizeof(float);
+}
+
+size_t scratch_bytes(int64_t M, int64_t V) {
+  const BwdBlocks b = bwd_blocks(M, V);
+  return (size_t)b.Mc * b.Vc * 2;
+}
+
+// Number of vocabulary splits: minimise (waves of units) x (tiles per unit);
+// ties go to fewer splits (fewer partials to merge).
+int choose_nsplit(int64_t n_mt, int64_t n_vt, int sms) {
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  const int64_t lim = std::min<int64_t>(n_vt, kNsplitMax);
+  for (int64_t ns = 1; ns <= lim; ++ns) {
+    const int64_t waves = cdiv(n_mt * ns, sms);
+    const int64_t cost = waves * cdiv(n_vt, ns);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = (int)ns;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  if (!g_encode) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace orpo
+
+using namespace orpo;
+
+extern "C" {
+
+size_t orpo_head_workspace_bytes(int64_t M, int64_t V, int64_t d) {
+  if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return 0;
+  return std::max(partial_bytes(M), scratch_bytes(M, V)) + 1024;
+}
+
+static void* align_ws(void* ws) {
+  uintptr_t p = reinterpret_cast<uintptr_t>(ws);
+  return reinterpret_cast<void*>((p + 1023) & ~uintptr_t(1023));
+}
+
+int orpo_head_fwd(const void* h, const void* W, const int32_t* targets, const uint8_t* mask, int64_t M, int64_t V,
+                  int64_t d, float softcap, float* logp, float* lse, void* workspace, size_t ws_bytes,
+                  int32_t* status, void* stream) {
+  if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return ORPO_ERR_SHAPE;
+  if (M == 0) return ORPO_OK;
+  if (!h || !W || !targets || !mask || !logp || !lse || !workspace || !status) return ORPO_ERR_NULL;
+  if (d % 8 != 0 || !aligned16(h) || !aligned16(W) || !aligned16(workspace)) return ORPO_ERR_ALIGN;
+  if (!isfinite(softcap)) return ORPO_ERR_ARG;
+  if (ws_bytes < orpo_head_workspace_bytes(M, V, d)) return ORPO_ERR_WORKSPACE;
+  int sms = 0;
+  if (int e = device_check(&sms)) return e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  FwdLaunch L;
+  const int64_t n_mt = cdiv(M, kBM), n_vt = cdiv(V, kBN);
+  if (!encode_map_2d(&L.mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, kBM) ||
+      !encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, kBN))
+    return ORPO_ERR_CUDA;
+  L.n_mt = (int)n_mt;
+  L.n_vt = (int)n_vt;
+  L.nsplit = choose_nsplit(n_mt, n_vt, sms);
+  L.kblocks = (int)cdiv(d, 64);
+  L.targets = targets;
+  L.mask = mask;
+  L.logp = logp;
+  L.lse = lse;
+  const int64_t Mpad = n_mt * kBM;
+  float* base = reinterpret_cast<float*>(align_ws(workspace));
+  L.part_m = base;
+  L.part_s = base + (size_t)kNsplitMax * Mpad;
+  L.M = (int)M;
+  L.Mpad = (int)Mpad;
+  L.V = (int)V;
+  L.softcap = softcap > 0.f ? softcap : 0.f;
+  L.status = status;
+  L.grid = (int)std::min<int64_t>(n_mt * L.nsplit, sms);
+  return launch_forward(L, st) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
+}
+
+int orpo_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int64_t M, int32_t n_pairs,
+              float lambda, float* out, float* ell, float* g, int32_t* status, void* stream) {
+  if (M < 0 || M > kMaxRows || n_pairs < 1 || n_pairs > ORPO_MAX_PAIRS) return ORPO_ERR_SHAPE;
+  if (!out || !ell || !status || (M > 0 && (!logp || !seq_id || !mask || !g))) return ORPO_ERR_NULL;
+  if (!isfinite(lambda) || lambda < 0.f) return ORPO_ERR_ARG;
+  int sms = 0;
+  if (int e = device_check(&sms)) return e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return launch_loss(logp, seq_id, mask, (int)M, n_pairs, lambda, out, ell, g, status, st) == cudaSuccess
+             ? ORPO_OK
+             : ORPO_ERR_CUDA;
+}
+
+int orpo_head_bwd(const void* h, const void* W, const int32_t* targets, const uint8_t* mask, const float* lse,
+                  const float* g, int64_t M, int64_t V, int64_t d, float softcap, float* dh, float* dW,
+                  int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
+  if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return ORPO_ERR_SHAPE;
+  if (!W || !dW || !status) return ORPO_ERR_NULL;
+  if (M > 0 && (!h || !targets || !mask || !lse || !g || !dh || !workspace)) return ORPO_ERR_NULL;
+  if (d % 8 != 0 || !aligned16(W) || !aligned16(dW) || (M > 0 && (!aligned16(h) || !aligned16(dh) ||
+                                                                  !aligned16(workspace))))
+    return ORPO_ERR_ALIGN;
+  if (!isfinite(softcap)) return ORPO_ERR_ARG;
+  if (M > 0 && ws_bytes < orpo_head_workspace_bytes(M, V, d)) return ORPO_ERR_WORKSPACE;
+  int sms = 0;
+  if (int e = device_check(&sms)) return e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    if (accumulate_dW) return ORPO_OK;
+    return cudaMemsetAsync(dW, 0, (size_t)V * d * sizeof(float), st) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
+  }
+
+  const BwdBlocks B = bwd_blocks(M, V);
+  void* S = align_ws(workspace);
+  RecLaunch R;
+  GemmLaunch G;
+  bool ok = encode_map_2d(&R.mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, kBM) &&
+            encode_map_2d(&R.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, kBN) &&
+            encode_map_2d(&R.ms_store, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, B.Vc * 2, 64, 32) &&
+            // gemm maps: 0 S K-major rows, 1 W MN-major, 2 S MN-major, 3 h MN-major, 4 dh, 5 dW
+            encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, B.Vc * 2, 64, kBM) &&
+            encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, 64) &&
+            encode_map_2d(&G.maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, B.Vc * 2, 64, 64) &&
+            encode_map_2d(&G.maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, 64) &&
+            encode_map_2d(&G.maps[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dh, d, M, d * 4, 32, 32) &&
+            encode_map_2d(&G.maps[5], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, d, V, d * 4, 32, 32);
+  if (!ok) return ORPO_ERR_CUDA;
+  G.status = status;
+  R.targets = targets;
+  R.mask = mask;
+  R.lse = lse;
+  R.g = g;
+  R.M = (int)M;
+  R.V = (int)V;
+  R.softcap = softcap > 0.f ? softcap : 0.f;
+  R.status = status;
+  R.kblocks = (int)cdiv(d, 64);
+  const int n_nt = (int)cdiv(d, kBN);
+
+  for (int64_t m0 = 0; m0 < M; m0 += B.Mc) {
+    const int64_t mc = std::min(B.Mc, M - m0);
+    const int n_mt = (int)cdiv(mc, kBM);
+    for (int64_t v0 = 0; v0 < V; v0 += B.Vc) {
+      const int64_t vc = std::min(B.Vc, V - v0);
+      const int n_vt = (int)cdiv(vc, kBN);
+      R.m0 = (int)m0;
+      R.v0 = (int)v0;
+      R.n_mt = n_mt;
+      R.n_vt = n_vt;
+      R.grid = (int)std::min<int64_t>((int64_t)n_mt * n_vt, sms);
+      if (launch_recompute(R, st) != cudaSuccess) return ORPO_ERR_CUDA;
+
+      GemmClassH cdw{};  // dW[v0 + ..] (+)= S^T h[m0 + ..]
+      cdw.a_map = 2, cdw.a_mn = 1, cdw.a_mn_base = 0, cdw.a_k_base = 0;
+      cdw.b_map = 3, cdw.b_mn = 1, cdw.b_mn_base = 0, cdw.b_k_base = (int)m0;
+      cdw.out_map = 5, cdw.out_row_base = (int)v0, cdw.out_col_base = 0;
+      cdw.reduce = (m0 > 0 || accumulate_dW) ? 1 : 0;
+      cdw.out_rows = (int)V, cdw.out_cols = (int)d;
+      cdw.n_mt = (int)cdiv(vc, kBM), cdw.n_nt = n_nt, cdw.kblocks = (int)cdiv(mc, 64);
+      cdw.mt_major = 0;
+      GemmClassH cdh{};  // dh[m0 + ..] (+)= S W[v0 + ..]
+      cdh.a_map = 0, cdh.a_mn = 0, cdh.a_mn_base = 0, cdh.a_k_base = 0;
+      cdh.b_map = 1, cdh.b_mn = 1, cdh.b_mn_base = 0, cdh.b_k_base = (int)v0;
+      cdh.out_map = 4, cdh.out_row_base = (int)m0, cdh.out_col_base = 0;
+      cdh.reduce = v0 > 0 ? 1 : 0;
+      cdh.out_rows = (int)M, cdh.out_cols = (int)d;
+      cdh.n_mt = n_mt, cdh.n_nt = n_nt, cdh.kblocks = (int)cdiv(vc, 64);
+      cdh.mt_major = 1;
+      // longer tiles first
+      if (cdw.kblocks >= cdh.kblocks) {
+        G.cls[0] = cdw;
+        G.cls[1] = cdh;
+      } else {
+        G.cls[0] = cdh;
+        G.cls[1] = cdw;
+      }
+      const int64_t units = (int64_t)cdw.n_mt * cdw.n_nt + (int64_t)cdh.n_mt * cdh.n_nt;
+      G.grid = (int)std::min<int64_t>(units, sms);
+      if (launch_gemm(G, st) != cudaSuccess) return ORPO_ERR_CUDA;
+    }
+  }
+  return ORPO_OK;
+}
+
+int orpo_debug_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int a_mn_major,
+                    int b_mn_major, int32_t* status, void* stream) {
+  if (M < 1 || N < 1 || K < 1 || M > kMaxRows || N > kMaxRows || K > kMaxRows) return ORPO_ERR_SHAPE;
+  if (!A || !B || !C || !status) return ORPO_ERR_NULL;
+  const int64_t a_inner = a_mn_major ? M : K, b_inner = b_mn_major ? N : K;
+  if (a_inner % 8 || b_inner % 8 || N % 4 || !aligned16(A) || !aligned16(B) || !aligned16(C))
+    return ORPO_ERR_ALIGN;
+  int sms = 0;
+  if (int e = device_check(&sms)) return e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  GemmLaunch G;
+  bool ok = a_mn_major ? encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, M, K, M * 2, 64, 64)
+                       : encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, K * 2, 64, kBM);
+  ok = ok && (b_mn_major ? encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, N * 2, 64, 64)
+                         : encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, K * 2, 64, kBN));
+  ok = ok && encode_map_2d(&G.maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, 32);
+  if (!ok) return ORPO_ERR_CUDA;
+  G.maps[3] = G.maps[4] = G.maps[5] = G.maps[0];
+  GemmClassH c{};
+  c.a_map = 0, c.a_mn = a_mn_major ? 1 : 0;
+  c.b_map = 1, c.b_mn = b_mn_major ? 1 : 0;
+  c.out_map = 2, c.reduce = 0, c.out_rows = (int)M, c.out_cols = (int)N;
+  c.n_mt = (int)cdiv(M, kBM), c.n_nt = (int)cdiv(N, kBN), c.kblocks = (int)cdiv(K, 64), c.mt_major = 1;
+  G.cls[0] = c;
+  G.cls[1] = GemmClassH{};
+  G.status = status;
+  G.grid = (int)std::min<int64_t>((int64_t)c.n_mt * c.n_nt, sms);
+  return launch_gemm(G, st) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
+}
+
+const char* orpo_status_string(int code) {
+  switch (code) {
+    case ORPO_OK: return "ok";
+    case ORPO_ERR_NULL: return "a required pointer is NULL";
+    case ORPO_ERR_SHAPE: return "M, V, d or n_pairs out of range";
+    case ORPO_ERR_ALIGN: return "pointer not 16-byte aligned or d not a multiple of 8";
+    case ORPO_ERR_ARG: return "softcap or lambda not finite, or lambda < 0";
+    case ORPO_ERR_WORKSPACE: return "workspace smaller than orpo_head_workspace_bytes()";
+    case ORPO_ERR_CUDA: return "CUDA runtime error";
+    case ORPO_ERR_UNSUPPORTED: return "current device is not compute capability 10.3";
+    default: break;
+  }
+  static thread_local char buf[160];
+  if (code < 16) return "unknown code";
+  buf[0] = 0;
+  const struct {
+    int bit;
+    const char* text;
+  } bits[] = {{ORPO_STATUS_TARGET, "target out of range"},
+              {ORPO_STATUS_SEQID, "bad sequence id"},
+              {ORPO_STATUS_EMPTY_SEQ, "empty sequence"},
+              {ORPO_STATUS_NONFINITE, "non-finite value"},
+              {ORPO_STATUS_TIMEOUT, "on-chip wait timed out"}};
+  for (const auto& b : bits) {
+    if (code & b.bit) {
+      if (buf[0]) strncat(buf, "; ", sizeof(buf) - strlen(buf) - 1);
+      strncat(buf, b.text, sizeof(buf) - strlen(buf) - 1);
+    }
+  }
+  return buf[0] ? buf : "unknown status";
+}
+
+}  // extern "C"

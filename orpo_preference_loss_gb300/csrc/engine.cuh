@@ -1,0 +1,277 @@
+// engine.cuh — persistent, warp-specialised tcgen05 GEMM pipeline shared by every
+// contraction of the head (forward logits, backward logit recompute, dh and dW).
+//
+// One CTA per SM.  Warp 0 issues TMA loads into a STAGES-deep shared-memory ring,
+// warp 1 issues tcgen05.mma (one thread) into a double-buffered TMEM accumulator
+// (2 x 256 fp32 columns = all 512 columns), warps 2..5 run the epilogue that the
+// kernel supplies.  Each accumulator tile is BM x BN = 128 x 256, built from BK = 64
+// wide k-blocks (128-byte swizzle rows) of bf16 operands.
+//
+// Operand staging in shared memory (per stage: A 16 KiB, B 32 KiB):
+//   K-major operand  [rows, K] with K contiguous: one TMA box {64 (K), rows};
+//                    rows at 128 B pitch, 8-row swizzle atoms 1024 B apart (SBO).
+//   MN-major operand [K, rows] with rows contiguous: rows/64 TMA boxes {64, 64},
+//                    each 64 k-rows x 128 B = 8 KiB; LBO = 8 KiB between 64-wide
+//                    column blocks, SBO = 1 KiB between 8-k-row groups.
+// Every wait is bounded: a wait that exceeds kWaitLimitNs sets ORPO_STATUS_TIMEOUT,
+// flags the CTA as aborted and every role drains its own in-flight work and returns.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace orpo {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int UMMA_K = 16;
+constexpr int EPI_WARPS = 4;
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int TMEM_COLS = 512;
+
+constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KiB
+constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KiB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t BOX_BYTES = 4096;                 // one 32-row x 128-byte epilogue staging box
+constexpr uint32_t STAGING_PER_WARP = 2 * BOX_BYTES;  // double-buffered
+constexpr uint32_t SMEM_STAGING_OFF = STAGES * STAGE_BYTES;
+constexpr uint32_t SMEM_CTL_OFF = SMEM_STAGING_OFF + EPI_WARPS * STAGING_PER_WARP;
+constexpr uint32_t SMEM_CTL_BYTES = 256;
+constexpr uint32_t SMEM_TOTAL = SMEM_CTL_OFF + SMEM_CTL_BYTES + 1024;  // + slack to align the base to 1 KiB
+
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far above any legitimate wait
+
+constexpr int32_t kStatusTimeout = 1 << 8;  // ORPO_STATUS_TIMEOUT
+
+struct SmemCtl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+static_assert(sizeof(SmemCtl) <= SMEM_CTL_BYTES, "control block too large");
+
+// How one operand tile is fetched for one k-block.
+struct Operand {
+  const CUtensorMap* map;
+  int mn_major;  // 0: K-major (K contiguous), 1: MN-major (rows contiguous)
+  int mn0;       // first row of the tile (coordinate along the MN dimension of the tensor)
+  int k0;        // first K coordinate of k-block 0
+};
+
+struct TileOps {
+  Operand a, b;
+  int kblocks;
+};
+
+__device__ __forceinline__ uint8_t* smem_base_aligned() {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uintptr_t p = reinterpret_cast<uintptr_t>(smem_raw);
+  p = (p + 1023) & ~uintptr_t(1023);
+  return reinterpret_cast<uint8_t*>(p);
+}
+
+// Bounded wait on an mbarrier phase.  Returns false on abort / timeout.
+__device__ __forceinline__ bool wait_phase(SmemCtl* ctl, uint64_t* bar, uint32_t parity, int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (ctl->abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(status, kStatusTimeout);
+        ctl->abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Wait used while draining after an abort: short limit, ignores the abort flag.
+__device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 200000000ull) return;
+  }
+}
+
+__device__ __forceinline__ void load_operand(const Operand& op, uint64_t* bar, uint8_t* dst, int rows, int kb) {
+  if (op.mn_major == 0) {
+    tma_load_2d(op.map, bar, dst, op.k0 + kb * BK, op.mn0);
+  } else {
+    const int kk = op.k0 + kb * BK;
+#pragma unroll 1
+    for (int c = 0; c < rows / 64; ++c) tma_load_2d(op.map, bar, dst + c * (BK * 128), op.mn0 + 64 * c, kk);
+  }
+}
+
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, int kk) {
+  // K-major: advance 16 elements (32 B) inside the swizzle row; MN-major: advance 16 k-rows (2 KiB)
+  return mn_major ? smem_desc_sw128(base + kk * (UMMA_K * 128), BK * 128, 1024)
+                  : smem_desc_sw128(base + kk * (UMMA_K * 2), 16, 1024);
+}
+
+// ---------------------------------------------------------------- producer (one thread)
+template <class Sched>
+__device__ void producer_role(const Sched& sched, uint8_t* smem, SmemCtl* ctl, int32_t* status) {
+  uint32_t it = 0;
+  bool ok = true;
+  const int nu = sched.num_units();
+  for (int u = blockIdx.x; ok && u < nu; u += gridDim.x) {
+    const int len = sched.unit_len(u);
+    for (int j = 0; ok && j < len; ++j) {
+      const TileOps t = sched.tile(u, j);
+      for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
+        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+        if (!wait_phase(ctl, &ctl->empty[s], ph ^ 1u, status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a_dst = smem + s * STAGE_BYTES;
+        uint8_t* b_dst = a_dst + A_BYTES;
+        mbar_arrive_expect_tx(&ctl->full[s], STAGE_BYTES);
+        load_operand(t.a, &ctl->full[s], a_dst, BM, kb);
+        load_operand(t.b, &ctl->full[s], b_dst, BN, kb);
+      }
+    }
+  }
+  if (!ok) {
+    // let the loads already issued land before the CTA can exit
+    const uint32_t first = it > STAGES ? it - STAGES : 0;
+    for (uint32_t k = first; k < it; ++k) drain_phase(&ctl->full[k % STAGES], (k / STAGES) & 1u);
+  }
+}
+
+// ---------------------------------------------------------------- MMA issuer (one thread)
+template <class Sched>
+__device__ void mma_role(const Sched& sched, uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base, int32_t* status) {
+  uint32_t it = 0, tcount = 0;
+  bool ok = true;
+  const uint32_t smem0 = smem_u32(smem);
+  const int nu = sched.num_units();
+  for (int u = blockIdx.x; ok && u < nu; u += gridDim.x) {
+    const int len = sched.unit_len(u);
+    for (int j = 0; ok && j < len; ++j, ++tcount) {
+      const TileOps t = sched.tile(u, j);
+      const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
+      if (!wait_phase(ctl, &ctl->acc_empty[buf], aph ^ 1u, status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * BN;
+      const uint32_t idesc = make_idesc_bf16(BM, BN, t.a.mn_major, t.b.mn_major);
+      for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
+        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+        if (!wait_phase(ctl, &ctl->full[s], ph, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_base = smem0 + s * STAGE_BYTES;
+        const uint32_t b_base = a_base + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+          umma_bf16(d_tmem, operand_desc(a_base, t.a.mn_major, kk), operand_desc(b_base, t.b.mn_major, kk), idesc,
+                    (kb | kk) != 0 ? 1u : 0u);
+        }
+        umma_commit(&ctl->empty[s]);  // frees the stage once these MMAs have read it
+      }
+      if (!ok) break;
+      umma_commit(&ctl->acc_full[buf]);  // accumulator ready for the epilogue
+    }
+  }
+  // make sure every issued MMA has finished before TMEM is released
+  umma_commit(&ctl->drain);
+  drain_phase(&ctl->drain, 0);
+}
+
+// ---------------------------------------------------------------- epilogue helpers
+
+// Waits until accumulator tile `tcount` is ready; returns its TMEM address for
+// this warp's 32 lanes (column 0 of the tile).
+__device__ __forceinline__ bool epi_acquire(SmemCtl* ctl, uint32_t tmem_base, uint32_t tcount, int warp,
+                                            int32_t* status, uint32_t* taddr) {
+  const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
+  if (!wait_phase(ctl, &ctl->acc_full[buf], aph, status)) return false;
+  tc_fence_after();
+  *taddr = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + buf * BN;
+  return true;
+}
+
+__device__ __forceinline__ void epi_release(SmemCtl* ctl, uint32_t tcount) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->acc_empty[tcount & 1u]);
+}
+
+// 32 fp32 values of one row -> 128-byte swizzled row `lane` of a 32 x 128 B staging box
+__device__ __forceinline__ void stage_row_f32(uint32_t box, int lane, const uint32_t (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t addr = box + lane * 128 + ((uint32_t)(j ^ (lane & 7)) << 4);
+    st_shared_v4(addr, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  }
+}
+
+// 64 bf16 values (32 packed words) of one row -> swizzled row `lane` of a staging box
+__device__ __forceinline__ void stage_row_bf16(uint32_t box, int lane, const uint32_t (&w)[32]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t addr = box + lane * 128 + ((uint32_t)(j ^ (lane & 7)) << 4);
+    st_shared_v4(addr, w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  }
+}
+
+// ---------------------------------------------------------------- CTA driver
+
+// Runs the three roles; `epilogue(smem, ctl, tmem_base, warp, lane)` is the kernel's epilogue loop.
+template <class Sched, class EpiFn>
+__device__ __forceinline__ void run_cta(const Sched& sched, int32_t* status, EpiFn&& epilogue) {
+  uint8_t* smem = smem_base_aligned();
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + SMEM_CTL_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl->acc_full[b], 1);
+      mbar_init(&ctl->acc_empty[b], EPI_WARPS);
+    }
+    mbar_init(&ctl->drain, 1);
+    ctl->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) producer_role(sched, smem, ctl, status);
+  } else if (warp == 1) {
+    if (lane == 0) mma_role(sched, smem, ctl, tmem_base, status);
+  } else {
+    epilogue(smem, ctl, tmem_base, warp, lane);
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace orpo

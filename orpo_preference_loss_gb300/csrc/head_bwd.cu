@@ -1,0 +1,319 @@
+// head_bwd.cu — backward of the flash-CCE head and the generic fp32-output GEMM.
+//
+// Fused-head spec, backward bullet: recompute the vocabulary tiles, rebuild the
+// softmax from the saved lse, form g * (onehot - softmax) * sech^2 and contract
+// it into dh (and, here, dW).  The "Steel flash-CCE — handoff" page accumulated
+// dh with float atomics across vocabulary blocks; this build instead streams the
+// bf16 logit gradient of one (row block, vocabulary block) through a bounded
+// workspace block S and contracts it with two large-K GEMMs per block:
+//   recompute kernel : S = bf16(dZ[m0:m0+Mc, v0:v0+Vc])             (K = d)
+//   gemm kernel      : dh[m0 rows]  (+)= S   W[v0 rows]             (K = Vc)
+//                      dW[v0 rows]  (+)= S^T h[m0 rows]             (K = Mc)
+// Each output tile is written by exactly one CTA per launch (TMA store, or TMA
+// reduce-add after the first block), so results are bitwise reproducible.
+#include "engine.cuh"
+#include "internal.h"
+
+namespace orpo {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ================================================================ recompute -> S
+struct RecSched {
+  const CUtensorMap* mh;
+  const CUtensorMap* mw;
+  int m0, v0, n_mt, n_vt, kblocks;
+  __device__ int num_units() const { return n_mt * n_vt; }
+  __device__ int unit_len(int) const { return 1; }
+  __device__ TileOps tile(int u, int) const {
+    const int vt = u / n_mt, mt = u - vt * n_mt;
+    TileOps t;
+    t.a = Operand{mh, 0, m0 + mt * BM, 0};
+    t.b = Operand{mw, 0, v0 + vt * BN, 0};
+    t.kblocks = kblocks;
+    return t;
+  }
+};
+
+struct RecArgs {
+  const int32_t* targets;
+  const uint8_t* mask;
+  const float* lse;
+  const float* g;
+  int M, V;
+  float softcap;
+  int32_t* status;
+};
+
+// dZ for 32 accumulator values of one row starting at vocabulary column col0;
+// writes 16 packed bf16 pairs into w[0..15].
+//   softcap on : z~ = c (1 - 2q), q = 1 / (1 + e^{2z/c}),  sech^2(z/c) = 4 q (1 - q)
+//   dZ = g sech^2 (onehot - 2^(x - lse2)),  x = z~ log2(e)
+__device__ __forceinline__ void dz_chunk(const uint32_t (&r)[32], int col0, int V, int y, float gval, float lse2,
+                                         bool cap, float K, float A, float B2, uint32_t* w) {
+  float dz[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float z = __uint_as_float(r[i]);
+    float x, gs;
+    if (cap) {
+      const float q = rcp_approx(1.f + ex2_approx(z * K));
+      x = fmaf(-B2, q, A);
+      gs = gval * (4.f * q * (1.f - q));
+    } else {
+      x = z * kLog2e;
+      gs = gval;
+    }
+    dz[i] = -gs * ex2_approx(x - lse2);
+  }
+  if ((unsigned)(y - col0) < 32u) {  // the target column lies in this chunk: add g * sech^2 there
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i == y - col0) {
+        float gs = gval;
+        if (cap) {
+          const float q = rcp_approx(1.f + ex2_approx(__uint_as_float(r[i]) * K));
+          gs = gval * (4.f * q * (1.f - q));
+        }
+        dz[i] += gs;
+      }
+    }
+  }
+  if (col0 + 32 > V) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i >= V) dz[i] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(dz[2 * i], dz[2 * i + 1]);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    rec_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mw,
+               const __grid_constant__ CUtensorMap ms, RecSched sched, RecArgs p) {
+  sched.mh = &mh;
+  sched.mw = &mw;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&mh);
+    tma_prefetch_desc(&mw);
+    tma_prefetch_desc(&ms);
+  }
+  run_cta(sched, p.status, [&](uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
+    const int q = warp & 3;
+    const uint32_t staging = smem_u32(smem + SMEM_STAGING_OFF + (warp - 2) * STAGING_PER_WARP);
+    const bool cap = p.softcap > 0.f;
+    const float K = cap ? 2.f * kLog2e / p.softcap : 0.f;
+    const float A = cap ? p.softcap * kLog2e : 0.f;
+    const float B2 = 2.f * A;
+    uint32_t tcount = 0, nstore = 0;
+    const int nu = sched.num_units();
+    for (int u = blockIdx.x; u < nu; u += gridDim.x, ++tcount) {
+      const int vt = u / sched.n_mt, mt = u - vt * sched.n_mt;
+      const int srow = mt * BM + 32 * q;  // first scratch row of this warp
+      const int row = sched.m0 + srow + lane;
+      float gval = 0.f, lse2 = 0.f;
+      int y = -1;
+      if (row < p.M && p.mask[row] != 0) {
+        gval = p.g[row];
+        y = p.targets[row];
+        if (y < 0 || y >= p.V) {
+          atomicOr(p.status, 1 << 4);
+          y = -1;
+        }
+        lse2 = p.lse[row] * kLog2e;
+      }
+      const bool warp_zero = __all_sync(0xffffffffu, gval == 0.f);
+      uint32_t taddr;
+      if (!epi_acquire(ctl, tmem_base, tcount, warp, p.status, &taddr)) break;
+      const int vcol0 = sched.v0 + vt * BN;  // global vocabulary column of the tile
+      uint32_t ra[32], rb[32];
+      if (!warp_zero) tmem_ld32(taddr, ra);
+#pragma unroll 1
+      for (int gi = 0; gi < BN / 64; ++gi) {
+        uint32_t w[32];
+        if (warp_zero) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = 0u;
+        } else {
+          tmem_ld_wait(ra);
+          tmem_ld32(taddr + gi * 64 + 32, rb);
+          dz_chunk(ra, vcol0 + gi * 64, p.V, y, gval, lse2, cap, K, A, B2, w);
+          tmem_ld_wait(rb);
+          if (gi + 1 < BN / 64) tmem_ld32(taddr + gi * 64 + 64, ra);
+          dz_chunk(rb, vcol0 + gi * 64 + 32, p.V, y, gval, lse2, cap, K, A, B2, w + 16);
+        }
+        const uint32_t box = staging + (nstore & 1u) * BOX_BYTES;
+        if (lane == 0) bulk_wait_group_read<1>();  // the store that used this buffer has read it
+        __syncwarp();
+        stage_row_bf16(box, lane, w);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&ms, smem + SMEM_STAGING_OFF + (warp - 2) * STAGING_PER_WARP + (nstore & 1u) * BOX_BYTES,
+                       vt * BN + gi * 64, srow);
+          bulk_commit_group();
+        }
+        ++nstore;
+      }
+      epi_release(ctl, tcount);
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  });
+}
+
+// ================================================================ fp32-output GEMM (dh, dW, diagnostic)
+struct GemmClass {
+  int a_map, a_mn, a_mn_base, a_k_base;
+  int b_map, b_mn, b_mn_base, b_k_base;
+  int out_map, out_row_base, out_col_base, reduce;
+  int out_rows, out_cols;
+  int n_mt, n_nt, kblocks;
+  int mt_major;
+};
+
+struct GemmSched {
+  const CUtensorMap* maps[6];
+  GemmClass cls[2];
+  __device__ int n0() const { return cls[0].n_mt * cls[0].n_nt; }
+  __device__ int num_units() const { return n0() + cls[1].n_mt * cls[1].n_nt; }
+  __device__ int unit_len(int) const { return 1; }
+  __device__ void decode(int u, int& k, int& mt, int& nt) const {
+    k = u < n0() ? 0 : 1;
+    const int v = k == 0 ? u : u - n0();
+    const GemmClass& c = cls[k];
+    if (c.mt_major) {
+      mt = v / c.n_nt;
+      nt = v - mt * c.n_nt;
+    } else {
+      nt = v / c.n_mt;
+      mt = v - nt * c.n_mt;
+    }
+  }
+  __device__ TileOps tile(int u, int) const {
+    int k, mt, nt;
+    decode(u, k, mt, nt);
+    const GemmClass& c = cls[k];
+    TileOps t;
+    t.a = Operand{maps[c.a_map], c.a_mn, c.a_mn_base + mt * BM, c.a_k_base};
+    t.b = Operand{maps[c.b_map], c.b_mn, c.b_mn_base + nt * BN, c.b_k_base};
+    t.kblocks = c.kblocks;
+    return t;
+  }
+};
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
+                const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
+                const __grid_constant__ CUtensorMap m4, const __grid_constant__ CUtensorMap m5, GemmSched sched,
+                int32_t* status) {
+  sched.maps[0] = &m0;
+  sched.maps[1] = &m1;
+  sched.maps[2] = &m2;
+  sched.maps[3] = &m3;
+  sched.maps[4] = &m4;
+  sched.maps[5] = &m5;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 6; ++i) tma_prefetch_desc(sched.maps[i]);
+  }
+  run_cta(sched, status, [&](uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
+    const int q = warp & 3;
+    uint8_t* stage_ptr = smem + SMEM_STAGING_OFF + (warp - 2) * STAGING_PER_WARP;
+    const uint32_t staging = smem_u32(stage_ptr);
+    uint32_t tcount = 0, nstore = 0;
+    const int nu = sched.num_units();
+    for (int u = blockIdx.x; u < nu; u += gridDim.x, ++tcount) {
+      int k, mt, nt;
+      sched.decode(u, k, mt, nt);
+      const GemmClass& c = sched.cls[k];
+      const CUtensorMap* out = sched.maps[c.out_map];
+      const int orow = c.out_row_base + mt * BM + 32 * q;
+      const int ocol0 = c.out_col_base + nt * BN;
+      uint32_t taddr;
+      if (!epi_acquire(ctl, tmem_base, tcount, warp, status, &taddr)) break;
+      if (orow < c.out_rows) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr, ra);
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ch += 2) {
+          tmem_ld_wait(ra);
+          tmem_ld32(taddr + (ch + 1) * 32, rb);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (h == 1) {
+              tmem_ld_wait(rb);
+              if (ch + 2 < BN / 32) tmem_ld32(taddr + (ch + 2) * 32, ra);
+            }
+            const int col = ocol0 + (ch + h) * 32;
+            if (col < c.out_cols) {
+              const uint32_t box = staging + (nstore & 1u) * BOX_BYTES;
+              if (lane == 0) bulk_wait_group_read<1>();
+              __syncwarp();
+              if (h == 0)
+                stage_row_f32(box, lane, ra);
+              else
+                stage_row_f32(box, lane, rb);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                const void* src = stage_ptr + (nstore & 1u) * BOX_BYTES;
+                if (c.reduce)
+                  tma_reduce_add_2d(out, src, col, orow);
+                else
+                  tma_store_2d(out, src, col, orow);
+                bulk_commit_group();
+              }
+              ++nstore;
+            }
+          }
+        }
+      }
+      epi_release(ctl, tcount);
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  });
+}
+
+}  // namespace
+
+cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st) {
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(rec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks};
+  RecArgs a{L.targets, L.mask, L.lse, L.g, L.M, L.V, L.softcap, L.status};
+  rec_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, L.ms_store, sched, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  GemmSched sched;
+  for (int i = 0; i < 6; ++i) sched.maps[i] = nullptr;
+  for (int k = 0; k < 2; ++k) {
+    const GemmClassH& h = L.cls[k];
+    sched.cls[k] = GemmClass{h.a_map,   h.a_mn,         h.a_mn_base,    h.a_k_base, h.b_map,    h.b_mn,
+                             h.b_mn_base, h.b_k_base,   h.out_map,      h.out_row_base, h.out_col_base, h.reduce,
+                             h.out_rows,  h.out_cols,   h.n_mt,         h.n_nt,     h.kblocks,  h.mt_major};
+  }
+  gemm_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.maps[0], L.maps[1], L.maps[2], L.maps[3], L.maps[4],
+                                                       L.maps[5], sched, L.status);
+  return cudaGetLastError();
+}
+
+}  // namespace orpo

@@ -1,0 +1,203 @@
+// head_fwd.cu — forward of the flash-CCE head.
+//
+// Design page "Training — design", §5.1 tier 4 (vocab-parallel grid with
+// per-block partials merged per row) and the fused-head spec's forward bullet
+// (online max / sum-exp over vocabulary tiles, softcap, target capture).
+//
+// Work unit = (row tile of 128, vocabulary split).  A CTA walks the 256-wide
+// vocabulary tiles of its split; for each tile the tensor cores build the
+// 128 x 256 fp32 logit block in TMEM, and the epilogue (one thread per row)
+// applies the softcap, folds the block into the row's running (max, sum-exp)
+// in base-2 units and captures the target logit.  At the end of the unit the
+// row's partial (max, sum) is written to the workspace; a small merge kernel
+// combines the splits into lse and logp.
+#include "engine.cuh"
+#include "internal.h"
+
+namespace orpo {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct FwdSched {
+  const CUtensorMap* mh;
+  const CUtensorMap* mw;
+  int n_mt, nsplit, n_vt, kblocks;
+  __device__ int num_units() const { return n_mt * nsplit; }
+  __device__ int vt_begin(int s) const { return (int)(((long long)s * n_vt) / nsplit); }
+  __device__ int unit_len(int u) const {
+    const int s = u / n_mt;
+    return vt_begin(s + 1) - vt_begin(s);
+  }
+  __device__ TileOps tile(int u, int j) const {
+    const int s = u / n_mt, mt = u - s * n_mt;
+    const int vt = vt_begin(s) + j;
+    TileOps t;
+    t.a = Operand{mh, 0, mt * BM, 0};
+    t.b = Operand{mw, 0, vt * BN, 0};
+    t.kblocks = kblocks;
+    return t;
+  }
+};
+
+struct FwdArgs {
+  const int32_t* targets;
+  const uint8_t* mask;
+  float* tgt;  // receives z~[t, y_t] (the logp buffer, finalised by the merge)
+  float* part_m;
+  float* part_s;
+  int M, Mpad, V;
+  float softcap;
+  int32_t* status;
+};
+
+// Per-row online softmax state of one epilogue thread, base-2 units.
+struct RowState {
+  float m, s;
+};
+
+// Fold 32 logits (raw fp32 accumulator bits) starting at column col0 into the row state.
+__device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, int V, int y, bool cap, float K,
+                                           float A, float B2, RowState& st, float* tgt_slot) {
+  if (col0 >= V) return;
+  float x[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float z = __uint_as_float(r[i]);
+    // softcap: z~ = c tanh(z/c) = c (1 - 2 / (1 + e^{2z/c})); in base-2 units x = A - B2 / (1 + 2^{zK})
+    x[i] = cap ? fmaf(-B2, rcp_approx(1.f + ex2_approx(z * K)), A) : z * kLog2e;
+  }
+  if (col0 + 32 > V) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i >= V) x[i] = -INFINITY;
+  }
+  if ((unsigned)(y - col0) < 32u) {
+    float v = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i == y - col0) v = x[i];
+    *tgt_slot = v * kLn2;
+  }
+  float m0 = fmaxf(x[0], x[1]), m1 = fmaxf(x[2], x[3]), m2 = fmaxf(x[4], x[5]), m3 = fmaxf(x[6], x[7]);
+#pragma unroll
+  for (int i = 8; i < 32; i += 8) {
+    m0 = fmaxf(m0, fmaxf(x[i], x[i + 1]));
+    m1 = fmaxf(m1, fmaxf(x[i + 2], x[i + 3]));
+    m2 = fmaxf(m2, fmaxf(x[i + 4], x[i + 5]));
+    m3 = fmaxf(m3, fmaxf(x[i + 6], x[i + 7]));
+  }
+  const float mnew = fmaxf(st.m, fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    a0 += ex2_approx(x[i] - mnew);
+    a1 += ex2_approx(x[i + 1] - mnew);
+    a2 += ex2_approx(x[i + 2] - mnew);
+    a3 += ex2_approx(x[i + 3] - mnew);
+  }
+  st.s = fmaf(st.s, ex2_approx(st.m - mnew), (a0 + a1) + (a2 + a3));
+  st.m = mnew;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mw, FwdSched sched,
+               FwdArgs p) {
+  sched.mh = &mh;
+  sched.mw = &mw;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&mh);
+    tma_prefetch_desc(&mw);
+  }
+  run_cta(sched, p.status, [&](uint8_t*, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
+    const int q = warp & 3;
+    const bool cap = p.softcap > 0.f;
+    const float K = cap ? 2.f * kLog2e / p.softcap : 0.f;
+    const float A = cap ? p.softcap * kLog2e : 0.f;
+    const float B2 = 2.f * A;
+    uint32_t tcount = 0;
+    const int nu = sched.num_units();
+    for (int u = blockIdx.x; u < nu; u += gridDim.x) {
+      const int s = u / sched.n_mt, mt = u - s * sched.n_mt;
+      const int row = mt * BM + 32 * q + lane;
+      int y = -1;
+      if (row < p.M && p.mask[row] != 0) y = p.targets[row];
+      float* tgt_slot = p.tgt + (row < p.M ? row : 0);
+      RowState st{-INFINITY, 0.f};
+      const int len = sched.unit_len(u);
+      const int vt0 = sched.vt_begin(s);
+      for (int j = 0; j < len; ++j, ++tcount) {
+        uint32_t taddr;
+        if (!epi_acquire(ctl, tmem_base, tcount, warp, p.status, &taddr)) return;
+        const int col_base = (vt0 + j) * BN;
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr, ra);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; c += 2) {
+          tmem_ld_wait(ra);
+          tmem_ld32(taddr + (c + 1) * 32, rb);
+          fold_chunk(ra, col_base + c * 32, p.V, y, cap, K, A, B2, st, tgt_slot);
+          tmem_ld_wait(rb);
+          if (c + 2 < BN / 32) tmem_ld32(taddr + (c + 2) * 32, ra);
+          fold_chunk(rb, col_base + (c + 1) * 32, p.V, y, cap, K, A, B2, st, tgt_slot);
+        }
+        epi_release(ctl, tcount);
+      }
+      p.part_m[(size_t)s * p.Mpad + row] = st.m;
+      p.part_s[(size_t)s * p.Mpad + row] = st.s;
+    }
+  });
+}
+
+// lse[t] = ln2 * (gM + log2 sum_k s_k 2^(m_k - gM));  logp[t] = z~[t,y_t] - lse[t] on response rows.
+__global__ void merge_kernel(const float* __restrict__ part_m, const float* __restrict__ part_s, int nsplit,
+                             int Mpad, int M, int V, const int32_t* __restrict__ targets,
+                             const uint8_t* __restrict__ mask, float* __restrict__ logp, float* __restrict__ lse,
+                             int32_t* status) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= M) return;
+  float gm = -INFINITY;
+  for (int k = 0; k < nsplit; ++k) gm = fmaxf(gm, part_m[(size_t)k * Mpad + t]);
+  float S = 0.f;
+  for (int k = 0; k < nsplit; ++k) S += part_s[(size_t)k * Mpad + t] * exp2f(part_m[(size_t)k * Mpad + t] - gm);
+  const float l = (gm + log2f(S)) * kLn2;
+  lse[t] = l;
+  int32_t err = 0;
+  if (!isfinite(l)) err |= 1 << 7;
+  float out = 0.f;
+  if (mask[t] != 0) {
+    const int y = targets[t];
+    if (y < 0 || y >= V)
+      err |= 1 << 4;
+    else
+      out = logp[t] - l;
+  }
+  logp[t] = out;
+  if (err) atomicOr(status, err);
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st) {
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  FwdSched sched{nullptr, nullptr, L.n_mt, L.nsplit, L.n_vt, L.kblocks};
+  FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M, L.Mpad, L.V, L.softcap, L.status};
+  fwd_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, sched, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int threads = 256;
+  merge_kernel<<<(L.M + threads - 1) / threads, threads, 0, st>>>(L.part_m, L.part_s, L.nsplit, L.Mpad, L.M, L.V,
+                                                                  L.targets, L.mask, L.logp, L.lse, L.status);
+  return cudaGetLastError();
+}
+
+}  // namespace orpo

@@ -1,0 +1,74 @@
+// internal.h — host-side declarations shared by the translation units of liborpo_head.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace orpo {
+
+// ---- tiling / blocking constants visible to the host
+constexpr int kBM = 128;          // rows per accumulator tile
+constexpr int kBN = 256;          // columns per accumulator tile
+constexpr int kNsplitMax = 64;    // most vocabulary splits of the forward
+constexpr int64_t kMcMax = 16384; // rows per backward block
+constexpr int64_t kScratchBudget = 256ll << 20;  // bytes of the bf16 dZ block
+
+// ---- forward
+struct FwdLaunch {
+  CUtensorMap mh, mw;  // h K-major box {64,128}; W K-major box {64,256}
+  int n_mt, nsplit, n_vt, kblocks;
+  const int32_t* targets;
+  const uint8_t* mask;
+  float* logp;
+  float* lse;
+  float* part_m;
+  float* part_s;
+  int M, Mpad, V;
+  float softcap;
+  int32_t* status;
+  int grid;
+};
+cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st);
+
+// ---- backward: recompute dZ for one (row block, vocab block) into the scratch
+struct RecLaunch {
+  CUtensorMap mh, mw, ms_store;  // h, W as in the forward; S store box {64,32}
+  int m0, v0, n_mt, n_vt, kblocks;
+  const int32_t* targets;
+  const uint8_t* mask;
+  const float* lse;
+  const float* g;
+  int M, V;
+  float softcap;
+  int32_t* status;
+  int grid;
+};
+cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st);
+
+// ---- generic two-class GEMM with an fp32 store / reduce-add epilogue
+struct GemmClassH {
+  int a_map, a_mn, a_mn_base, a_k_base;
+  int b_map, b_mn, b_mn_base, b_k_base;
+  int out_map, out_row_base, out_col_base, reduce;
+  int out_rows, out_cols;  // valid extent of the output tensor
+  int n_mt, n_nt, kblocks;
+  int mt_major;
+};
+struct GemmLaunch {
+  CUtensorMap maps[6];
+  GemmClassH cls[2];
+  int32_t* status;
+  int grid;
+};
+cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st);
+
+// ---- loss
+cudaError_t launch_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int M, int P, float lam,
+                        float* out, float* ell, float* g, int32_t* status, cudaStream_t st);
+
+// ---- tensor maps (driver entry point fetched through the runtime)
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+}  // namespace orpo

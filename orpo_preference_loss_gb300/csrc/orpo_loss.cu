@@ -1,0 +1,244 @@
+// orpo_loss.cu — the ORPO objective over per-token log-probs.
+//
+// Design page "Training — design", §1 "The objective": per sequence the mean
+// response log-prob l_s, per pair the log-odds x = (l_w - l_r) - (log1mexp(l_w) -
+// log1mexp(l_r)), loss = mean_p(-l_w + lambda * softplus(-x)), and the metrics
+// loss / nll / or / accuracy / margin.  The gradient with respect to each
+// token's logp is written in closed form (d x / d l_w = 1 / (1 - e^{l_w}), the
+// "1/(1-P)" factor of §4), divided by the sequence's response-token count.
+//
+// One CTA of 1024 threads.  Rows are split into 1024 contiguous chunks; each
+// thread sums the runs of equal sequence id inside its chunk in fp64.  A run
+// strictly inside a chunk is a whole sequence (ids are non-decreasing); the
+// first and last runs of each chunk are partial and are combined per sequence
+// by one warp in a fixed lane/butterfly order, so the result is bitwise
+// reproducible.  Per-pair arithmetic is fp64; outputs are fp32.
+#include <math.h>
+
+#include "internal.h"
+
+namespace orpo {
+
+namespace {
+
+constexpr int T = 1024;
+constexpr int32_t kSeqErr = 1 << 5, kEmptyErr = 1 << 6, kNonfiniteErr = 1 << 7;
+
+struct LossSmem {
+  int head_sid[T], tail_sid[T], first_sid[T], last_sid[T];
+  int head_cnt[T], tail_cnt[T];
+  double head_sum[T], tail_sum[T];
+  double red[5][T / 32];
+  int err;
+};
+// followed by: double seq_sum[S]; int seq_cnt[S]; double G[S]
+
+__device__ __forceinline__ double log1mexp_d(double x) {
+  // log(1 - e^x), x <= 0; two branches at -ln 2 (Maechler 2012)
+  return x > -0.6931471805599453 ? log(-expm1(x)) : log1p(-exp(x));
+}
+
+__device__ __forceinline__ double softplus_d(double x) { return fmax(x, 0.0) + log1p(exp(-fabs(x))); }
+
+__device__ __forceinline__ double sigmoid_d(double x) {
+  const double e = exp(-fabs(x));
+  return x >= 0 ? 1.0 / (1.0 + e) : e / (1.0 + e);
+}
+
+__global__ void __launch_bounds__(T, 1)
+    loss_kernel(const float* __restrict__ logp, const int32_t* __restrict__ seq_id,
+                const uint8_t* __restrict__ mask, int M, int P, float lam_f, float* __restrict__ out,
+                float* __restrict__ ell, float* __restrict__ g, int32_t* status) {
+  extern __shared__ __align__(16) uint8_t raw[];
+  LossSmem& sm = *reinterpret_cast<LossSmem*>(raw);
+  const int S = 2 * P;
+  double* seq_sum = reinterpret_cast<double*>(raw + sizeof(LossSmem));
+  int* seq_cnt = reinterpret_cast<int*>(seq_sum + S);
+  double* G = reinterpret_cast<double*>(raw + sizeof(LossSmem) + (size_t)S * 8 + (((size_t)S * 4 + 7) & ~size_t(7)));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const double lam = (double)lam_f;
+
+  if (tid == 0) sm.err = 0;
+  for (int s = tid; s < S; s += T) {
+    seq_sum[s] = 0.0;
+    seq_cnt[s] = 0;
+  }
+  __syncthreads();
+
+  // ---- phase 1: runs inside the contiguous chunk of this thread
+  int err = 0;
+  {
+    const int chunk = (M + T - 1) / T;
+    const int t0 = min(M, tid * chunk), t1 = min(M, t0 + chunk);
+    int cur = -1, cnt = 0, nruns = 0, last = -1, first = -1;
+    double sum = 0.0;
+    int hs = -1, hc = 0, ts = -1, tc = 0;
+    double hsum = 0.0, tsum = 0.0;
+    for (int t = t0; t < t1; ++t) {
+      const int sid = seq_id[t];
+      if (sid == -1) continue;
+      if (sid < -1 || sid >= S) {
+        err |= kSeqErr;
+        continue;
+      }
+      if (sid < last) err |= kSeqErr;
+      if (sid != cur) {
+        if (cur >= 0) {
+          if (nruns == 0) {
+            hs = cur, hsum = sum, hc = cnt;
+          } else {
+            seq_sum[cur] = sum;  // a run strictly inside the chunk is the whole sequence
+            seq_cnt[cur] = cnt;
+          }
+          ++nruns;
+        }
+        cur = sid;
+        sum = 0.0;
+        cnt = 0;
+      }
+      if (mask[t] != 0) {
+        sum += (double)logp[t];
+        ++cnt;
+      }
+      last = sid;
+      if (first < 0) first = sid;
+    }
+    if (cur >= 0) {
+      if (nruns == 0) {
+        hs = cur, hsum = sum, hc = cnt;
+      } else {
+        ts = cur, tsum = sum, tc = cnt;
+        // the previously flushed run was written as interior; if it was the head it is in hs
+      }
+    }
+    sm.head_sid[tid] = hs;
+    sm.head_sum[tid] = hsum;
+    sm.head_cnt[tid] = hc;
+    sm.tail_sid[tid] = ts;
+    sm.tail_sum[tid] = tsum;
+    sm.tail_cnt[tid] = tc;
+    sm.first_sid[tid] = first;
+    sm.last_sid[tid] = last;
+  }
+  __syncthreads();
+
+  // ---- phase 1b: ids must not decrease across chunk boundaries
+  if (sm.first_sid[tid] >= 0) {
+    for (int j = tid - 1; j >= 0; --j) {
+      if (sm.last_sid[j] >= 0) {
+        if (sm.last_sid[j] > sm.first_sid[tid]) err |= kSeqErr;
+        break;
+      }
+    }
+  }
+
+  // ---- phase 2: add the partial head / tail runs of every chunk to their sequence
+  for (int s = warp; s < S; s += T / 32) {
+    double acc = 0.0;
+    int c = 0;
+    for (int i = lane; i < T; i += 32) {
+      if (sm.head_sid[i] == s) {
+        acc += sm.head_sum[i];
+        c += sm.head_cnt[i];
+      }
+      if (sm.tail_sid[i] == s) {
+        acc += sm.tail_sum[i];
+        c += sm.tail_cnt[i];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      c += __shfl_xor_sync(0xffffffffu, c, o);
+    }
+    if (lane == 0) {
+      seq_sum[s] += acc;
+      seq_cnt[s] += c;
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 3: per-sequence means
+  for (int s = tid; s < S; s += T) {
+    const int n = seq_cnt[s];
+    double l = NAN;
+    if (n == 0)
+      err |= kEmptyErr;
+    else
+      l = seq_sum[s] / (double)n;
+    seq_sum[s] = l;
+    ell[s] = (float)l;
+  }
+  __syncthreads();
+
+  // ---- phase 4: per pair value, metrics and gradient
+  double c_loss = 0.0, c_nll = 0.0, c_or = 0.0, c_acc = 0.0, c_mar = 0.0;
+  for (int p = tid; p < P; p += T) {
+    const double lw = seq_sum[2 * p], lr = seq_sum[2 * p + 1];
+    const double x = (lw - lr) - (log1mexp_d(lw) - log1mexp_d(lr));
+    const double lor = softplus_d(-x);
+    const double sg = sigmoid_d(-x);
+    const double inv_w = -1.0 / expm1(lw), inv_r = -1.0 / expm1(lr);
+    const double Gw = (-1.0 - lam * sg * inv_w) / (double)P;
+    const double Gr = (lam * sg * inv_r) / (double)P;
+    if (lw > 0.0 || lr > 0.0 || !isfinite(x) || !isfinite(Gw) || !isfinite(Gr) || !isfinite(lor) ||
+        !isfinite(lw))
+      err |= kNonfiniteErr;
+    G[2 * p] = Gw;
+    G[2 * p + 1] = Gr;
+    c_loss += -lw + lam * lor;
+    c_nll += -lw;
+    c_or += lor;
+    c_acc += lw > lr ? 1.0 : 0.0;
+    c_mar += x;
+  }
+  // fixed-order block reduction of the five sums
+  double v[5] = {c_loss, c_nll, c_or, c_acc, c_mar};
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+    if (lane == 0) sm.red[k][warp] = v[k];
+  }
+  if (err) atomicOr(&sm.err, err);
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+      double a = sm.red[k][lane];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      if (lane == 0) out[k] = (float)(a / (double)P);
+    }
+    if (lane == 0 && sm.err) atomicOr(status, sm.err);
+  }
+
+  // ---- phase 5: per-token gradient
+  for (int t = tid; t < M; t += T) {
+    const int sid = seq_id[t];
+    float gv = 0.f;
+    if (sid >= 0 && sid < S && mask[t] != 0) {
+      const int n = seq_cnt[sid];
+      if (n > 0) gv = (float)(G[sid] / (double)n);
+    }
+    g[t] = gv;
+  }
+}
+
+}  // namespace
+
+size_t loss_smem_bytes(int P) {
+  const size_t S = 2 * (size_t)P;
+  return sizeof(LossSmem) + S * 8 + ((S * 4 + 7) & ~size_t(7)) + S * 8;
+}
+
+cudaError_t launch_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int M, int P, float lam,
+                        float* out, float* ell, float* g, int32_t* status, cudaStream_t st) {
+  const size_t smem = loss_smem_bytes(P);
+  cudaError_t e = cudaFuncSetAttribute(loss_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  loss_kernel<<<1, T, smem, st>>>(logp, seq_id, mask, M, P, lam, out, ell, g, status);
+  return cudaGetLastError();
+}
+
+}  // namespace orpo
