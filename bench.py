@@ -1,0 +1,359 @@
+#!/usr/bin/env python3
+"""Benchmark of the flash-CCE ORPO head: forward + ORPO loss + backward per step.
+
+Default workload: the Gemma-e4b-shaped head (M 8192 response tokens = 16 pairs
+x 2 x 256, d 2560, V 262144, softcap 30, lambda 0.1, peaked synthetic h).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  `value` is whole-job tokens/s with inputs
+resident in HBM, device-timed with CUDA events over exactly K steps;
+`e2e` is the same metric with the host->device copy of each step's inputs and
+the device->host read of its loss inside the timed region.  `--impl reference`
+times the float64 CPU oracle (the repository's only other implementation of
+the method) on a bounded sample of the same workload.  Under torchrun each rank
+runs an independent replica (weak scaling; the path has no exchange step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ORPO head fwd+bwd tokens/s and TFLOP/s (6·M·V·d) vs bf16 peak; peak extra GB"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="e4b", choices=["tiny", "small", "e4b", "largev", "ragged"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return (float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                float(p["hbm_gbs"]), "measured")
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, 1700.0, FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_config(w):
+    return {"workload": f"{w.name}: M {w.M} rows ({w.n_pairs} pairs), d {w.d}, V {w.V}, softcap {w.softcap:g}, "
+                        f"lambda {w.lam:g}",
+            "M": w.M, "d": w.d, "V": w.V, "pairs": w.n_pairs, "softcap": w.softcap, "lambda": w.lam,
+            "l2": "inputs larger than L2 (W alone is %.2f GB)" % (w.V * w.d * 2 / 1e9)}
+
+
+# ---------------------------------------------------------------- clocks during the timed region
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        load = [s for s in sm if s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle (CPU baseline / reference arm)
+def oracle_sample(w, rows_per_seq):
+    """One pair of the workload with each response cut to its first rows_per_seq rows."""
+    sel = []
+    for s in (0, 1):
+        idx = np.where(w.seq_id == s)[0][:rows_per_seq]
+        sel.append(idx)
+    idx = np.concatenate(sel)
+    return idx
+
+
+def run_oracle_sample(w, idx, W64):
+    import oracle
+    h = oracle.bf16_bits_to_f64(w.h[idx])
+    t0 = time.perf_counter()
+    oracle.full_chain(h, W64, w.targets[idx], w.mask[idx], w.seq_id[idx], 1, w.lam, w.softcap)
+    return time.perf_counter() - t0
+
+
+def oracle_weights(w):
+    import oracle
+    return oracle.bf16_bits_to_f64(w.W)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def reference_arm(args, w, rank, world):
+    """Times the float64 oracle, as it stands, on a bounded sample of the workload."""
+    if rank != 0:
+        return
+    rows = 64 if w.V * w.d > 1e8 else 256
+    idx = oracle_sample(w, rows)
+    W64 = oracle_weights(w)
+    for _ in range(args.warmup):
+        run_oracle_sample(w, idx, W64)
+    tot = 0.0
+    for _ in range(args.steps):
+        tot += run_oracle_sample(w, idx, W64)
+    v = len(idx) * args.steps / tot
+    cfg = workload_config(w)
+    sample = (f"one pair, first {rows} rows of each response ({len(idx)} tokens), full V and d, "
+              "float64 forward + loss + backward")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def ours(args, w, rank, world, local):
+    import torch
+    import torch.distributed as dist
+
+    import orpo_preference_loss_gb300 as orpo
+    from orpo_preference_loss_gb300 import build as orpo_build
+
+    orpo_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    M, d, V, P = w.M, w.d, w.V, w.n_pairs
+    host = {
+        "h": torch.from_numpy(np.ascontiguousarray(w.h).view(np.int16)).pin_memory(),
+        "W": torch.from_numpy(np.ascontiguousarray(w.W).view(np.int16)).pin_memory(),
+        "targets": torch.from_numpy(np.ascontiguousarray(w.targets)).pin_memory(),
+        "mask": torch.from_numpy(np.ascontiguousarray(w.mask)).pin_memory(),
+        "seq_id": torch.from_numpy(np.ascontiguousarray(w.seq_id)).pin_memory(),
+    }
+    t = {k: v.to(dev) for k, v in host.items()}
+    h_bf = t["h"].view(torch.bfloat16)
+    W_bf = t["W"].view(torch.bfloat16)
+    logp = torch.empty(M, dtype=torch.float32, device=dev)
+    lse = torch.empty(M, dtype=torch.float32, device=dev)
+    out = torch.empty(5, dtype=torch.float32, device=dev)
+    ell = torch.empty(2 * P, dtype=torch.float32, device=dev)
+    g = torch.empty(M, dtype=torch.float32, device=dev)
+    dh = torch.empty((M, d), dtype=torch.float32, device=dev)
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    mem_before = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    ws = torch.empty(orpo.orpo_head_workspace_bytes(M, V, d), dtype=torch.uint8, device=dev)
+
+    def step():
+        orpo.orpo_head_fwd(h_bf, W_bf, t["targets"], t["mask"], w.softcap, logp, lse, ws, status)
+        orpo.orpo_loss(logp, t["seq_id"], t["mask"], P, w.lam, out, ell, g, status)
+        orpo.orpo_head_bwd(h_bf, W_bf, t["targets"], t["mask"], lse, g, w.softcap, dh, dW, False, ws, status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    peak_extra = torch.cuda.max_memory_allocated(dev) - mem_before
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {orpo.orpo_status_string(st)}")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- device-timed region: inputs resident in HBM
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    orpo.orpo_profile_start()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prof = orpo.orpo_profile_stop()
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        x = torch.tensor([ms], device=dev)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        ms = float(x.item())
+    ms_step = ms / args.steps
+    value = world * M * args.steps / (ms / 1e3)
+
+    # ---- end to end through host buffers: H2D inputs, step, D2H loss/metrics
+    e2e = None
+    if not args.no_e2e:
+        out_host = torch.empty(5, dtype=torch.float32).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        barrier()
+        torch.cuda.synchronize()
+        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        for _ in range(args.steps):
+            for k in host:
+                t[k].copy_(host[k], non_blocking=True)
+            step()
+            out_host.copy_(out, non_blocking=True)
+        e3.record(stream)
+        torch.cuda.synchronize()
+        ms2 = e2.elapsed_time(e3)
+        if world > 1:
+            x = torch.tensor([ms2], device=dev)
+            dist.all_reduce(x, op=dist.ReduceOp.MAX)
+            ms2 = float(x.item())
+        e2e = {"value": world * M * args.steps / (ms2 / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {orpo.orpo_status_string(st)}")
+
+    if rank != 0:
+        return
+
+    burst, sustained, hbm, src = peaks()
+    flops_step = 6.0 * M * V * d
+    tflops = world * flops_step * args.steps / (ms / 1e3) / 1e12
+    # per-kernel algorithmic flops over the timed region (dense contractions each kernel computes)
+    kflops = {"fwd_logits": 2.0 * M * V * d * args.steps,
+              "bwd_recompute": 2.0 * M * V * d * args.steps,
+              "bwd_grad_gemm": 4.0 * M * V * d * args.steps}
+    kernels = {}
+    for name, (kms, cnt) in prof.items():
+        if cnt == 0:
+            continue
+        e = {"launches": cnt, "ms_total": kms, "ms_per_launch": kms / cnt, "share": kms / ms}
+        if name in kflops and kms > 0:
+            e["tflops"] = kflops[name] / (kms / 1e3) / 1e12
+        kernels[name] = e
+    dom = max((k for k in kernels if k in kflops), key=lambda k: kernels[k]["ms_total"])
+    per_launch_flops = kflops[dom] / kernels[dom]["launches"]
+    achieved = per_launch_flops / (kernels[dom]["ms_per_launch"] / 1e3) / 1e12
+    traffic = None
+    roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
+            "frac": achieved / sustained, "traffic": traffic,
+            "peak_source": f"{src} bf16 sustained (MEASURED_PEAKS.json bf16_tflops_sustained)"}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+            "tflops": tflops, "frac_of_peak": tflops / sustained, "frac_of_burst_peak": tflops / burst,
+            "peak_extra_gb": peak_extra / 1e9, "e2e": e2e, "gpu_launches": sum(v["launches"] for v in
+                                                                               kernels.values()),
+            "kernels": kernels, "roofline": roof, "clocks": clk}
+    if world == 1 and not args.no_cpu_baseline:
+        idx = oracle_sample(w, 256)
+        del t, host
+        secs = run_oracle_sample(w, idx, oracle_weights(w))
+        line["cpu_baseline"] = {"value": len(idx) / secs, "unit": "tokens/s", "cores": cpu_cores(),
+                                "kind": "oracle",
+                                "sample": f"one pair, first 256 rows of each response ({len(idx)} tokens), "
+                                          "full V and d, float64 forward + loss + backward, "
+                                          f"{secs:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    import workloads
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = workloads.make(args.workload)
+        reference_arm(args, w, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = workloads.make(args.workload)
+    try:
+        ours(args, w, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -160,6 +160,20 @@ const char* orpo_status_string(int code);
 int orpo_debug_gemm(const void* A_bf16, const void* B_bf16, float* C, int64_t M, int64_t N,
                     int64_t K, int a_mn_major, int b_mn_major, int32_t* status, void* stream);
 
+/*
+ * Diagnostic: device time of the library's own launches (no counterpart on
+ * the pages).  Between orpo_profile_start() and orpo_profile_stop(), every
+ * kernel the library launches is bracketed by two CUDA events on its stream.
+ * orpo_profile_stop() waits for those events and writes, for kernel kinds
+ * 0 .. nkinds-1 (names from orpo_profile_kind_name: fwd_logits, fwd_merge,
+ * orpo_loss, bwd_recompute, bwd_grad_gemm, debug_gemm), the summed milliseconds
+ * into ms[] and the launch count into count[] (host arrays).  Events are
+ * host-side objects pooled inside the library; no device memory is used.
+ */
+int orpo_profile_start(void);
+int orpo_profile_stop(double* ms, int64_t* count, int nkinds);
+const char* orpo_profile_kind_name(int kind);
+
 #ifdef __cplusplus
 }
 #endif

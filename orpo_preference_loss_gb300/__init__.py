@@ -19,6 +19,7 @@ from . import build as _build
 __all__ = [
     "OrpoError", "load", "lib_path", "orpo_head_workspace_bytes", "orpo_head_fwd", "orpo_loss",
     "orpo_head_bwd", "orpo_status_string", "orpo_debug_gemm", "OrpoHead", "STATUS_BITS",
+    "orpo_profile_start", "orpo_profile_stop",
 ]
 
 STATUS_BITS = {"target": 1 << 4, "seqid": 1 << 5, "empty": 1 << 6, "nonfinite": 1 << 7, "timeout": 1 << 8}
@@ -59,6 +60,12 @@ def load():
     L.orpo_status_string.restype = ctypes.c_char_p
     L.orpo_debug_gemm.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, vp]
     L.orpo_debug_gemm.restype = ctypes.c_int
+    L.orpo_profile_start.argtypes = []
+    L.orpo_profile_start.restype = ctypes.c_int
+    L.orpo_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), ctypes.c_int]
+    L.orpo_profile_stop.restype = ctypes.c_int
+    L.orpo_profile_kind_name.argtypes = [ctypes.c_int]
+    L.orpo_profile_kind_name.restype = ctypes.c_char_p
     _lib = L
     return L
 
@@ -157,6 +164,21 @@ def orpo_debug_gemm(A, B, C, M, N, K, a_mn_major, b_mn_major, status, stream=Non
     _dev(C, "C", (torch.float32,), (M, N))
     _check(load().orpo_debug_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(a_mn_major), int(b_mn_major),
                                   _ptr(status), _stream(stream)), "orpo_debug_gemm")
+
+
+PROFILE_KINDS = 6
+
+
+def orpo_profile_start():
+    _check(load().orpo_profile_start(), "orpo_profile_start")
+
+
+def orpo_profile_stop():
+    """Per kernel kind: {name: (total_ms, launches)} for the launches since orpo_profile_start()."""
+    ms = (ctypes.c_double * PROFILE_KINDS)()
+    cnt = (ctypes.c_int64 * PROFILE_KINDS)()
+    _check(load().orpo_profile_stop(ms, cnt, PROFILE_KINDS), "orpo_profile_stop")
+    return {load().orpo_profile_kind_name(k).decode(): (ms[k], int(cnt[k])) for k in range(PROFILE_KINDS)}
 
 
 class OrpoHead:

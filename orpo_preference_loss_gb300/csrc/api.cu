@@ -273,7 +273,7 @@ int orpo_head_bwd(const void* h, const void* W, const int32_t* targets, const ui
       }
       const int64_t units = (int64_t)cdw.n_mt * cdw.n_nt + (int64_t)cdh.n_mt * cdh.n_nt;
       G.grid = (int)std::min<int64_t>(units, sms);
-      if (launch_gemm(G, st) != cudaSuccess) return ORPO_ERR_CUDA;
+      if (launch_gemm(G, st, K_GEMM) != cudaSuccess) return ORPO_ERR_CUDA;
     }
   }
   return ORPO_OK;
@@ -306,7 +306,7 @@ int orpo_debug_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N
   G.cls[1] = GemmClassH{};
   G.status = status;
   G.grid = (int)std::min<int64_t>((int64_t)c.n_mt * c.n_nt, sms);
-  return launch_gemm(G, st) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
+  return launch_gemm(G, st, K_DEBUG) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
 }
 
 const char* orpo_status_string(int code) {

@@ -290,11 +290,13 @@ cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st) {
   }
   RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks};
   RecArgs a{L.targets, L.mask, L.lse, L.g, L.M, L.V, L.softcap, L.status};
+  prof_begin(K_REC, st);
   rec_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, L.ms_store, sched, a);
+  prof_end(K_REC, st);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
+cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -311,8 +313,10 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st) {
                              h.b_mn_base, h.b_k_base,   h.out_map,      h.out_row_base, h.out_col_base, h.reduce,
                              h.out_rows,  h.out_cols,   h.n_mt,         h.n_nt,     h.kblocks,  h.mt_major};
   }
+  prof_begin(kind, st);
   gemm_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.maps[0], L.maps[1], L.maps[2], L.maps[3], L.maps[4],
                                                        L.maps[5], sched, L.status);
+  prof_end(kind, st);
   return cudaGetLastError();
 }
 

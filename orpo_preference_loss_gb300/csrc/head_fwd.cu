@@ -191,12 +191,16 @@ cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st) {
   }
   FwdSched sched{nullptr, nullptr, L.n_mt, L.nsplit, L.n_vt, L.kblocks};
   FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M, L.Mpad, L.V, L.softcap, L.status};
+  prof_begin(K_FWD, st);
   fwd_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, sched, a);
+  prof_end(K_FWD, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int threads = 256;
+  prof_begin(K_MERGE, st);
   merge_kernel<<<(L.M + threads - 1) / threads, threads, 0, st>>>(L.part_m, L.part_s, L.nsplit, L.Mpad, L.M, L.V,
                                                                   L.targets, L.mask, L.logp, L.lse, L.status);
+  prof_end(K_MERGE, st);
   return cudaGetLastError();
 }
 

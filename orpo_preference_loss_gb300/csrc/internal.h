@@ -7,6 +7,11 @@
 
 namespace orpo {
 
+// ---- launch timing (profile.cu); no-ops unless orpo_profile_start() was called
+enum KernelKind { K_FWD = 0, K_MERGE, K_LOSS, K_REC, K_GEMM, K_DEBUG, K_NKINDS };
+void prof_begin(int kind, cudaStream_t st);
+void prof_end(int kind, cudaStream_t st);
+
 // ---- tiling / blocking constants visible to the host
 constexpr int kBM = 128;          // rows per accumulator tile
 constexpr int kBN = 256;          // columns per accumulator tile
@@ -61,7 +66,7 @@ struct GemmLaunch {
   int32_t* status;
   int grid;
 };
-cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st);
+cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind);
 
 // ---- loss
 cudaError_t launch_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int M, int P, float lam,

@@ -237,7 +237,9 @@ cudaError_t launch_loss(const float* logp, const int32_t* seq_id, const uint8_t*
   const size_t smem = loss_smem_bytes(P);
   cudaError_t e = cudaFuncSetAttribute(loss_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  prof_begin(K_LOSS, st);
   loss_kernel<<<1, T, smem, st>>>(logp, seq_id, mask, M, P, lam, out, ell, g, status);
+  prof_end(K_LOSS, st);
   return cudaGetLastError();
 }
 
