@@ -59,7 +59,8 @@ enum {
   ORPO_ERR_ARG = 4,         /* softcap / lambda not finite, or lambda < 0 */
   ORPO_ERR_WORKSPACE = 5,   /* ws_bytes < orpo_head_workspace_bytes(M, V, d) */
   ORPO_ERR_CUDA = 6,        /* a CUDA runtime call or a launch failed */
-  ORPO_ERR_UNSUPPORTED = 7  /* the current device is not compute capability 10.3 */
+  ORPO_ERR_UNSUPPORTED = 7, /* the current device is not compute capability 10.3 */
+  ORPO_ERR_TOO_LARGE = 8     /* M exceeds ORPO_FWD_STATIC_MAX_ROWS (orpo_head_fwd_static only) */
 };
 
 /* device-detected status bits (OR-ed into *status) */
@@ -159,6 +160,34 @@ const char* orpo_status_string(int code);
  */
 int orpo_debug_gemm(const void* A_bf16, const void* B_bf16, float* C, int64_t M, int64_t N,
                     int64_t K, int a_mn_major, int b_mn_major, int32_t* status, void* stream);
+
+/*
+ * Forward for callers that cannot allocate device memory (no counterpart on
+ * the pages; a packaging variant of orpo_head_fwd).  Some callers hold only
+ * their inputs and outputs: a plugin or custom-call hook of another framework
+ * whose enqueue step receives buffers but is not allowed to allocate, or a
+ * service that fixes its device-memory budget at start-up and forbids
+ * cudaMalloc afterwards.  This entry point computes exactly what orpo_head_fwd
+ * computes, but keeps the per-split softmax partials in a fixed 4 MiB array
+ * that lives inside the library (every GPU that loads the library holds it
+ * until the process exits) instead of in a caller workspace.  It allocates
+ * nothing and calls no allocating routine.
+ *   - Limit: M <= ORPO_FWD_STATIC_MAX_ROWS; larger M returns ORPO_ERR_TOO_LARGE
+ *     and launches nothing.  Large M may use fewer vocabulary splits than
+ *     orpo_head_fwd (results agree to rounding).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents; nothing in it needs to start at zero (every entry read was
+ *     written by the same call).  Calls whose GPU work overlaps in time (other
+ *     streams, other host threads) race on it: order them on one stream.
+ * Arguments, outputs and device status bits are those of orpo_head_fwd.
+ */
+#define ORPO_FWD_STATIC_MAX_ROWS 65536
+int orpo_head_fwd_static(const void* h_bf16, const void* W_bf16, const int32_t* targets,
+                         const uint8_t* mask, int64_t M, int64_t V, int64_t d, float softcap,
+                         float* logp, float* lse, int32_t* status, void* stream);
 
 /*
  * Diagnostic: device time of the library's own launches (no counterpart on

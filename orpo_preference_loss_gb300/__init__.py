@@ -19,7 +19,7 @@ from . import build as _build
 __all__ = [
     "OrpoError", "load", "lib_path", "orpo_head_workspace_bytes", "orpo_head_fwd", "orpo_loss",
     "orpo_head_bwd", "orpo_status_string", "orpo_debug_gemm", "OrpoHead", "STATUS_BITS",
-    "orpo_profile_start", "orpo_profile_stop",
+    "orpo_profile_start", "orpo_profile_stop", "orpo_head_fwd_static",
 ]
 
 STATUS_BITS = {"target": 1 << 4, "seqid": 1 << 5, "empty": 1 << 6, "nonfinite": 1 << 7, "timeout": 1 << 8}
@@ -60,6 +60,8 @@ def load():
     L.orpo_status_string.restype = ctypes.c_char_p
     L.orpo_debug_gemm.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, vp]
     L.orpo_debug_gemm.restype = ctypes.c_int
+    L.orpo_head_fwd_static.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp, vp, vp, vp]
+    L.orpo_head_fwd_static.restype = ctypes.c_int
     L.orpo_profile_start.argtypes = []
     L.orpo_profile_start.restype = ctypes.c_int
     L.orpo_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), ctypes.c_int]
@@ -124,6 +126,26 @@ def orpo_head_fwd(h, W, targets, mask, softcap, logp, lse, workspace, status, st
     _check(load().orpo_head_fwd(_ptr(h), _ptr(W), _ptr(targets), _ptr(mask), M, V, d, float(softcap),
                                 _ptr(logp), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(status),
                                 _stream(stream)), "orpo_head_fwd")
+
+
+FWD_STATIC_MAX_ROWS = 65536
+
+
+def orpo_head_fwd_static(h, W, targets, mask, softcap, logp, lse, status, stream=None):
+    """orpo_head_fwd without a workspace argument, for callers that may not allocate
+    device memory: the split partials use a fixed array inside the library."""
+    M, d = h.shape
+    V = W.shape[0]
+    _dev(h, "h", BF16)
+    _dev(W, "W", BF16, (V, d))
+    _dev(targets, "targets", (torch.int32,), (M,))
+    _dev(mask, "mask", (torch.uint8, torch.bool), (M,))
+    _dev(logp, "logp", (torch.float32,), (M,))
+    _dev(lse, "lse", (torch.float32,), (M,))
+    _dev(status, "status", (torch.int32,))
+    _check(load().orpo_head_fwd_static(_ptr(h), _ptr(W), _ptr(targets), _ptr(mask), M, V, d, float(softcap),
+                                       _ptr(logp), _ptr(lse), _ptr(status), _stream(stream)),
+           "orpo_head_fwd_static")
 
 
 def orpo_loss(logp, seq_id, mask, n_pairs, lam, out, ell, g, status, stream=None):

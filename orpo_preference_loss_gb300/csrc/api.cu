@@ -319,6 +319,7 @@ const char* orpo_status_string(int code) {
     case ORPO_ERR_WORKSPACE: return "workspace smaller than orpo_head_workspace_bytes()";
     case ORPO_ERR_CUDA: return "CUDA runtime error";
     case ORPO_ERR_UNSUPPORTED: return "current device is not compute capability 10.3";
+    case ORPO_ERR_TOO_LARGE: return "M exceeds ORPO_FWD_STATIC_MAX_ROWS for orpo_head_fwd_static";
     default: break;
   }
   static thread_local char buf[160];
@@ -342,3 +343,79 @@ const char* orpo_status_string(int code) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- forward without a caller workspace
+//
+// For callers that may not allocate: the forward's per-split (max, sum-exp)
+// partials live in this fixed device array instead of a workspace.  Capacity
+// 2^20 floats (4 MiB): 2 * nsplit * Mpad floats, with nsplit capped so that the
+// largest accepted M (65536 rows, Mpad 65536) still has 8 splits.
+namespace orpo {
+namespace {
+
+constexpr int64_t kStaticFloats = 1 << 20;
+static __device__ __align__(256) float g_fwd_static_partials[kStaticFloats];
+
+struct StaticAddr {
+  float* ptr = nullptr;
+};
+StaticAddr g_static_addr[64];
+std::mutex g_static_mu;
+
+// Device address of the array for the current device (looked up once per device).
+int static_partials(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ORPO_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_addr[dev].ptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fwd_static_partials) != cudaSuccess || !p) return ORPO_ERR_CUDA;
+    g_static_addr[dev].ptr = static_cast<float*>(p);
+  }
+  *out = g_static_addr[dev].ptr;
+  return ORPO_OK;
+}
+
+}  // namespace
+}  // namespace orpo
+
+extern "C" int orpo_head_fwd_static(const void* h, const void* W, const int32_t* targets, const uint8_t* mask,
+                                    int64_t M, int64_t V, int64_t d, float softcap, float* logp, float* lse,
+                                    int32_t* status, void* stream) {
+  if (M < 0 || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return ORPO_ERR_SHAPE;
+  if (M > ORPO_FWD_STATIC_MAX_ROWS) return ORPO_ERR_TOO_LARGE;
+  if (M == 0) return ORPO_OK;
+  if (!h || !W || !targets || !mask || !logp || !lse || !status) return ORPO_ERR_NULL;
+  if (d % 8 != 0 || !aligned16(h) || !aligned16(W)) return ORPO_ERR_ALIGN;
+  if (!isfinite(softcap)) return ORPO_ERR_ARG;
+  int sms = 0;
+  if (int e = device_check(&sms)) return e;
+  float* part = nullptr;
+  if (int e = static_partials(&part)) return e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  FwdLaunch L;
+  const int64_t n_mt = cdiv(M, kBM), n_vt = cdiv(V, kBN);
+  const int64_t Mpad = n_mt * kBM;
+  if (!encode_map_2d(&L.mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, kBM) ||
+      !encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, kBN))
+    return ORPO_ERR_CUDA;
+  const int cap = (int)std::max<int64_t>(1, kStaticFloats / (2 * Mpad));
+  L.n_mt = (int)n_mt;
+  L.n_vt = (int)n_vt;
+  L.nsplit = std::min(choose_nsplit(n_mt, n_vt, sms), cap);
+  L.kblocks = (int)cdiv(d, 64);
+  L.targets = targets;
+  L.mask = mask;
+  L.logp = logp;
+  L.lse = lse;
+  L.part_m = part;
+  L.part_s = part + (size_t)L.nsplit * Mpad;
+  L.M = (int)M;
+  L.Mpad = (int)Mpad;
+  L.V = (int)V;
+  L.softcap = softcap > 0.f ? softcap : 0.f;
+  L.status = status;
+  L.grid = (int)std::min<int64_t>(n_mt * L.nsplit, sms);
+  return launch_forward(L, st) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
+}
