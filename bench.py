@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--M", type=int, default=None, help="shrink the workload's rows (profiling cases)")
+    ap.add_argument("--V", type=int, default=None, help="shrink the vocabulary (profiling cases)")
+    ap.add_argument("--d", type=int, default=None, help="change the hidden size (profiling cases)")
     return ap.parse_args()
 
 
@@ -338,7 +341,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        w = workloads.make(args.workload)
+        w = workloads.make(args.workload, M=args.M, d=args.d, V=args.V)
         reference_arm(args, w, rank, world)
         return
     if world > 1:
@@ -346,7 +349,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    w = workloads.make(args.workload)
+    w = workloads.make(args.workload, M=args.M, d=args.d, V=args.V)
     try:
         ours(args, w, rank, world, local)
     finally:
