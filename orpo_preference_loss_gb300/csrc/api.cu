@@ -83,10 +83,21 @@ size_t partial_bytes(int64_t M) {
   return (size_t)2 * kNsplitMax * Mpad * sizeof(float);
 }
 
+// Row pitch of the dZ block in elements: 64 past the width, so that rows of the
+// block (Vc is a power of two for the common vocabularies) do not all start on the
+// same power-of-two address offsets.
+inline int64_t scratch_pitch(const BwdBlocks& b) { return b.Vc + 64; }
+
 size_t scratch_bytes(int64_t M, int64_t V) {
   const BwdBlocks b = bwd_blocks(M, V);
-  return (size_t)b.Mc * b.Vc * 2;
+  return (size_t)b.Mc * scratch_pitch(b) * 2;
 }
+
+// Unit counters of the dh/dW GEMM launches (dynamic scheduling): a fixed ring of
+// kCounters slots; launch k uses slot k % kCounters and the ring is zeroed
+// (stream-ordered) before every kCounters-th launch.
+constexpr int kCounters = 4096;
+constexpr size_t kCounterBytes = kCounters * sizeof(int);
 
 // Number of vocabulary splits: minimise (waves of units) x (tiles per unit);
 // ties go to fewer splits (fewer partials to merge).
@@ -120,6 +131,19 @@ bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, u
   return r == CUDA_SUCCESS;
 }
 
+bool encode_map_mn3d(CUtensorMap* map, const void* base, uint64_t mn, uint64_t k, uint64_t row_bytes,
+                     uint32_t chunks) {
+  if (!g_encode || mn % 64 != 0) return false;
+  const cuuint64_t dims[3] = {64, k, mn / 64};
+  const cuuint64_t strides[2] = {row_bytes, 128};
+  const cuuint32_t box[3] = {64, 64, chunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace orpo
 
 using namespace orpo;
@@ -128,7 +152,7 @@ extern "C" {
 
 size_t orpo_head_workspace_bytes(int64_t M, int64_t V, int64_t d) {
   if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return 0;
-  return std::max(partial_bytes(M), scratch_bytes(M, V)) + 1024;
+  return std::max(partial_bytes(M), scratch_bytes(M, V) + kCounterBytes) + 1024;
 }
 
 static void* align_ws(void* ws) {
@@ -209,16 +233,22 @@ int orpo_head_bwd(const void* h, const void* W, const int32_t* targets, const ui
 
   const BwdBlocks B = bwd_blocks(M, V);
   void* S = align_ws(workspace);
+  int* counters = reinterpret_cast<int*>(static_cast<uint8_t*>(S) + scratch_bytes(M, V));
+  int64_t launch = 0;
+  const int64_t sp = scratch_pitch(B);
+  const bool d64 = d % 64 == 0;  // MN-major h / W fetched with one 3-D box per stage
   RecLaunch R;
   GemmLaunch G;
   bool ok = encode_map_2d(&R.mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, kBM) &&
             encode_map_2d(&R.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, kBN) &&
-            encode_map_2d(&R.ms_store, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, B.Vc * 2, 64, 32) &&
+            encode_map_2d(&R.ms_store, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, sp * 2, 64, 32) &&
             // gemm maps: 0 S K-major rows, 1 W MN-major, 2 S MN-major, 3 h MN-major, 4 dh, 5 dW
-            encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, B.Vc * 2, 64, kBM) &&
-            encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, 64) &&
-            encode_map_2d(&G.maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, B.Vc * 2, 64, 64) &&
-            encode_map_2d(&G.maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, 64) &&
+            encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, sp * 2, 64, kBM) &&
+            (d64 ? encode_map_mn3d(&G.maps[1], W, d, V, d * 2, kBN / 64)
+                 : encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, 64)) &&
+            encode_map_mn3d(&G.maps[2], S, B.Vc, B.Mc, sp * 2, kBM / 64) &&
+            (d64 ? encode_map_mn3d(&G.maps[3], h, d, M, d * 2, kBN / 64)
+                 : encode_map_2d(&G.maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, 64)) &&
             encode_map_2d(&G.maps[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dh, d, M, d * 4, 32, 32) &&
             encode_map_2d(&G.maps[5], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, d, V, d * 4, 32, 32);
   if (!ok) return ORPO_ERR_CUDA;
@@ -248,16 +278,16 @@ int orpo_head_bwd(const void* h, const void* W, const int32_t* targets, const ui
       if (launch_recompute(R, st) != cudaSuccess) return ORPO_ERR_CUDA;
 
       GemmClassH cdw{};  // dW[v0 + ..] (+)= S^T h[m0 + ..]
-      cdw.a_map = 2, cdw.a_mn = 1, cdw.a_mn_base = 0, cdw.a_k_base = 0;
-      cdw.b_map = 3, cdw.b_mn = 1, cdw.b_mn_base = 0, cdw.b_k_base = (int)m0;
+      cdw.a_map = 2, cdw.a_mn = 2, cdw.a_mn_base = 0, cdw.a_k_base = 0;
+      cdw.b_map = 3, cdw.b_mn = d64 ? 2 : 1, cdw.b_mn_base = 0, cdw.b_k_base = (int)m0;
       cdw.out_map = 5, cdw.out_row_base = (int)v0, cdw.out_col_base = 0;
       cdw.reduce = (m0 > 0 || accumulate_dW) ? 1 : 0;
       cdw.out_rows = (int)V, cdw.out_cols = (int)d;
       cdw.n_mt = (int)cdiv(vc, kBM), cdw.n_nt = n_nt, cdw.kblocks = (int)cdiv(mc, 64);
-      cdw.mt_major = 0;
+      cdw.mt_major = 1;  // CTAs running together share one column slab of S; h stays in L2
       GemmClassH cdh{};  // dh[m0 + ..] (+)= S W[v0 + ..]
       cdh.a_map = 0, cdh.a_mn = 0, cdh.a_mn_base = 0, cdh.a_k_base = 0;
-      cdh.b_map = 1, cdh.b_mn = 1, cdh.b_mn_base = 0, cdh.b_k_base = (int)v0;
+      cdh.b_map = 1, cdh.b_mn = d64 ? 2 : 1, cdh.b_mn_base = 0, cdh.b_k_base = (int)v0;
       cdh.out_map = 4, cdh.out_row_base = (int)m0, cdh.out_col_base = 0;
       cdh.reduce = v0 > 0 ? 1 : 0;
       cdh.out_rows = (int)M, cdh.out_cols = (int)d;
@@ -273,6 +303,9 @@ int orpo_head_bwd(const void* h, const void* W, const int32_t* targets, const ui
       }
       const int64_t units = (int64_t)cdw.n_mt * cdw.n_nt + (int64_t)cdh.n_mt * cdh.n_nt;
       G.grid = (int)std::min<int64_t>(units, sms);
+      if (launch % kCounters == 0 && cudaMemsetAsync(counters, 0, kCounterBytes, st) != cudaSuccess)
+        return ORPO_ERR_CUDA;
+      G.counter = counters + (launch++ % kCounters);
       if (launch_gemm(G, st, K_GEMM) != cudaSuccess) return ORPO_ERR_CUDA;
     }
   }
@@ -290,20 +323,26 @@ int orpo_debug_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N
   if (int e = device_check(&sms)) return e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   GemmLaunch G;
-  bool ok = a_mn_major ? encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, M, K, M * 2, 64, 64)
-                       : encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, K * 2, 64, kBM);
-  ok = ok && (b_mn_major ? encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, N * 2, 64, 64)
-                         : encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, K * 2, 64, kBN));
+  // MN-major operands whose contiguous extent is a multiple of 64 use the one-box 3-D fetch
+  const int a_mode = a_mn_major ? (M % 64 == 0 ? 2 : 1) : 0;
+  const int b_mode = b_mn_major ? (N % 64 == 0 ? 2 : 1) : 0;
+  bool ok = a_mode == 2   ? encode_map_mn3d(&G.maps[0], A, M, K, M * 2, kBM / 64)
+            : a_mode == 1 ? encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, M, K, M * 2, 64, 64)
+                          : encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, K * 2, 64, kBM);
+  ok = ok && (b_mode == 2   ? encode_map_mn3d(&G.maps[1], B, N, K, N * 2, kBN / 64)
+              : b_mode == 1 ? encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, N * 2, 64, 64)
+                            : encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, K * 2, 64, kBN));
   ok = ok && encode_map_2d(&G.maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, 32);
   if (!ok) return ORPO_ERR_CUDA;
   G.maps[3] = G.maps[4] = G.maps[5] = G.maps[0];
   GemmClassH c{};
-  c.a_map = 0, c.a_mn = a_mn_major ? 1 : 0;
-  c.b_map = 1, c.b_mn = b_mn_major ? 1 : 0;
+  c.a_map = 0, c.a_mn = a_mode;
+  c.b_map = 1, c.b_mn = b_mode;
   c.out_map = 2, c.reduce = 0, c.out_rows = (int)M, c.out_cols = (int)N;
   c.n_mt = (int)cdiv(M, kBM), c.n_nt = (int)cdiv(N, kBN), c.kblocks = (int)cdiv(K, 64), c.mt_major = 1;
   G.cls[0] = c;
   G.cls[1] = GemmClassH{};
+  G.counter = nullptr;
   G.status = status;
   G.grid = (int)std::min<int64_t>((int64_t)c.n_mt * c.n_nt, sms);
   return launch_gemm(G, st, K_DEBUG) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;

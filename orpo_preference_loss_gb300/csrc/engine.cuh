@@ -43,6 +43,7 @@ constexpr uint32_t SMEM_TOTAL = SMEM_CTL_OFF + SMEM_CTL_BYTES + 1024;  // + slac
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far above any legitimate wait
 
 constexpr int32_t kStatusTimeout = 1 << 8;  // ORPO_STATUS_TIMEOUT
+constexpr int RING = 4;                     // unit indices in flight between the roles (dynamic feed)
 
 struct SmemCtl {
   uint64_t full[STAGES];
@@ -50,15 +51,66 @@ struct SmemCtl {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
+  uint64_t unit_full[RING];
+  uint64_t unit_empty[RING];
+  volatile int unit_ring[RING];
   uint32_t tmem_base;
   volatile int abort_flag;
 };
+
+// Source of work units.  Static: CTA b takes units b, b + G, b + 2G, ...
+// Dynamic (counter != nullptr): the producer thread claims the next unit with
+// an atomic add on a zeroed global counter and hands its index to the MMA and
+// epilogue warps through a RING-deep shared-memory ring; index -1 ends the
+// stream.  Every unit is still computed by exactly one CTA.
+struct Feed {
+  int* counter;
+  int nu;
+};
+
+__device__ __forceinline__ bool wait_phase(SmemCtl* ctl, uint64_t* bar, uint32_t parity, int32_t* status);
+
+// Producer side: returns the next unit, -1 when done, -2 on abort.
+__device__ __forceinline__ int feed_produce(const Feed& f, SmemCtl* ctl, uint32_t i, int32_t* status) {
+  if (f.counter == nullptr) {
+    const long long u = (long long)blockIdx.x + (long long)i * gridDim.x;
+    return u < f.nu ? (int)u : -1;
+  }
+  const uint32_t r = i % RING, ph = (i / RING) & 1u;
+  if (!wait_phase(ctl, &ctl->unit_empty[r], ph ^ 1u, status)) return -2;
+  int u = atomicAdd(f.counter, 1);
+  if (u >= f.nu) u = -1;
+  ctl->unit_ring[r] = u;
+  mbar_arrive(&ctl->unit_full[r]);
+  return u;
+}
+
+// Consumer side (the MMA thread, or a whole epilogue warp): same sequence as the producer's.
+__device__ __forceinline__ int feed_consume(const Feed& f, SmemCtl* ctl, uint32_t i, int32_t* status,
+                                            bool whole_warp) {
+  if (f.counter == nullptr) {
+    const long long u = (long long)blockIdx.x + (long long)i * gridDim.x;
+    return u < f.nu ? (int)u : -1;
+  }
+  const uint32_t r = i % RING, ph = (i / RING) & 1u;
+  if (!wait_phase(ctl, &ctl->unit_full[r], ph, status)) return -2;
+  const int u = ctl->unit_ring[r];
+  if (whole_warp) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->unit_empty[r]);
+  } else {
+    mbar_arrive(&ctl->unit_empty[r]);
+  }
+  return u;
+}
 static_assert(sizeof(SmemCtl) <= SMEM_CTL_BYTES, "control block too large");
 
 // How one operand tile is fetched for one k-block.
 struct Operand {
   const CUtensorMap* map;
-  int mn_major;  // 0: K-major (K contiguous), 1: MN-major (rows contiguous)
+  int mn_major;  // 0: K-major (K contiguous); 1: MN-major, one 2-D box {64, 64} per 64-wide column block;
+                 // 2: MN-major, all column blocks in one 3-D box {64, 64, rows/64} (map dims
+                 //    {64, K, MN/64}, strides {pitch, 128 B}; needs MN % 64 == 0)
   int mn0;       // first row of the tile (coordinate along the MN dimension of the tensor)
   int k0;        // first K coordinate of k-block 0
 };
@@ -103,6 +155,8 @@ __device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ void load_operand(const Operand& op, uint64_t* bar, uint8_t* dst, int rows, int kb) {
   if (op.mn_major == 0) {
     tma_load_2d(op.map, bar, dst, op.k0 + kb * BK, op.mn0);
+  } else if (op.mn_major == 2) {
+    tma_load_3d(op.map, bar, dst, 0, op.k0 + kb * BK, op.mn0 / 64);
   } else {
     const int kk = op.k0 + kb * BK;
 #pragma unroll 1
@@ -118,11 +172,15 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, in
 
 // ---------------------------------------------------------------- producer (one thread)
 template <class Sched>
-__device__ void producer_role(const Sched& sched, uint8_t* smem, SmemCtl* ctl, int32_t* status) {
+__device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* smem, SmemCtl* ctl, int32_t* status) {
   uint32_t it = 0;
   bool ok = true;
-  const int nu = sched.num_units();
-  for (int u = blockIdx.x; ok && u < nu; u += gridDim.x) {
+  for (uint32_t i = 0; ok; ++i) {
+    const int u = feed_produce(feed, ctl, i, status);
+    if (u < 0) {
+      ok = (u == -1);
+      break;
+    }
     const int len = sched.unit_len(u);
     for (int j = 0; ok && j < len; ++j) {
       const TileOps t = sched.tile(u, j);
@@ -149,12 +207,14 @@ __device__ void producer_role(const Sched& sched, uint8_t* smem, SmemCtl* ctl, i
 
 // ---------------------------------------------------------------- MMA issuer (one thread)
 template <class Sched>
-__device__ void mma_role(const Sched& sched, uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base, int32_t* status) {
+__device__ void mma_role(const Sched& sched, const Feed& feed, uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base,
+                         int32_t* status) {
   uint32_t it = 0, tcount = 0;
   bool ok = true;
   const uint32_t smem0 = smem_u32(smem);
-  const int nu = sched.num_units();
-  for (int u = blockIdx.x; ok && u < nu; u += gridDim.x) {
+  for (uint32_t i = 0; ok; ++i) {
+    const int u = feed_consume(feed, ctl, i, status, false);
+    if (u < 0) break;
     const int len = sched.unit_len(u);
     for (int j = 0; ok && j < len; ++j, ++tcount) {
       const TileOps t = sched.tile(u, j);
@@ -165,7 +225,7 @@ __device__ void mma_role(const Sched& sched, uint8_t* smem, SmemCtl* ctl, uint32
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
-      const uint32_t idesc = make_idesc_bf16(BM, BN, t.a.mn_major, t.b.mn_major);
+      const uint32_t idesc = make_idesc_bf16(BM, BN, t.a.mn_major != 0, t.b.mn_major != 0);
       for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
         if (!wait_phase(ctl, &ctl->full[s], ph, status)) {
@@ -177,7 +237,7 @@ __device__ void mma_role(const Sched& sched, uint8_t* smem, SmemCtl* ctl, uint32
         const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-          umma_bf16(d_tmem, operand_desc(a_base, t.a.mn_major, kk), operand_desc(b_base, t.b.mn_major, kk), idesc,
+          umma_bf16(d_tmem, operand_desc(a_base, t.a.mn_major != 0, kk), operand_desc(b_base, t.b.mn_major != 0, kk), idesc,
                     (kb | kk) != 0 ? 1u : 0u);
         }
         umma_commit(&ctl->empty[s]);  // frees the stage once these MMAs have read it
@@ -230,9 +290,10 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t box, int lane, const uin
 
 // ---------------------------------------------------------------- CTA driver
 
-// Runs the three roles; `epilogue(smem, ctl, tmem_base, warp, lane)` is the kernel's epilogue loop.
+// Runs the three roles; `epilogue(smem, ctl, tmem_base, warp, lane)` is the kernel's epilogue loop,
+// which walks the units with feed_consume(feed, ctl, i, status, true).
 template <class Sched, class EpiFn>
-__device__ __forceinline__ void run_cta(const Sched& sched, int32_t* status, EpiFn&& epilogue) {
+__device__ __forceinline__ void run_cta(const Sched& sched, const Feed& feed, int32_t* status, EpiFn&& epilogue) {
   uint8_t* smem = smem_base_aligned();
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + SMEM_CTL_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -246,6 +307,10 @@ __device__ __forceinline__ void run_cta(const Sched& sched, int32_t* status, Epi
       mbar_init(&ctl->acc_empty[b], EPI_WARPS);
     }
     mbar_init(&ctl->drain, 1);
+    for (int r = 0; r < RING; ++r) {
+      mbar_init(&ctl->unit_full[r], 1);
+      mbar_init(&ctl->unit_empty[r], 1 + EPI_WARPS);
+    }
     ctl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -259,9 +324,9 @@ __device__ __forceinline__ void run_cta(const Sched& sched, int32_t* status, Epi
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer_role(sched, smem, ctl, status);
+    if (lane == 0) producer_role(sched, feed, smem, ctl, status);
   } else if (warp == 1) {
-    if (lane == 0) mma_role(sched, smem, ctl, tmem_base, status);
+    if (lane == 0) mma_role(sched, feed, smem, ctl, tmem_base, status);
   } else {
     epilogue(smem, ctl, tmem_base, warp, lane);
   }

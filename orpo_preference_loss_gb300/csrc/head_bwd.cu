@@ -100,7 +100,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&mw);
     tma_prefetch_desc(&ms);
   }
-  run_cta(sched, p.status, [&](uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
+  const Feed feed{nullptr, sched.num_units()};
+  run_cta(sched, feed, p.status, [&](uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
     const int q = warp & 3;
     const uint32_t staging = smem_u32(smem + SMEM_STAGING_OFF + (warp - 2) * STAGING_PER_WARP);
     const bool cap = p.softcap > 0.f;
@@ -108,8 +109,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float A = cap ? p.softcap * kLog2e : 0.f;
     const float B2 = 2.f * A;
     uint32_t tcount = 0, nstore = 0;
-    const int nu = sched.num_units();
-    for (int u = blockIdx.x; u < nu; u += gridDim.x, ++tcount) {
+    for (uint32_t i = 0;; ++i, ++tcount) {
+      const int u = feed_consume(feed, ctl, i, p.status, true);
+      if (u < 0) break;
       const int vt = u / sched.n_mt, mt = u - vt * sched.n_mt;
       const int srow = mt * BM + 32 * q;  // first scratch row of this warp
       const int row = sched.m0 + srow + lane;
@@ -177,6 +179,17 @@ struct GemmClass {
 struct GemmSched {
   const CUtensorMap* maps[6];
   GemmClass cls[2];
+  // constant-index selection keeps the pointer table in registers (no local-memory copy)
+  __device__ __forceinline__ const CUtensorMap* map(int i) const {
+    switch (i) {
+      case 0: return maps[0];
+      case 1: return maps[1];
+      case 2: return maps[2];
+      case 3: return maps[3];
+      case 4: return maps[4];
+      default: return maps[5];
+    }
+  }
   __device__ int n0() const { return cls[0].n_mt * cls[0].n_nt; }
   __device__ int num_units() const { return n0() + cls[1].n_mt * cls[1].n_nt; }
   __device__ int unit_len(int) const { return 1; }
@@ -197,8 +210,8 @@ struct GemmSched {
     decode(u, k, mt, nt);
     const GemmClass& c = cls[k];
     TileOps t;
-    t.a = Operand{maps[c.a_map], c.a_mn, c.a_mn_base + mt * BM, c.a_k_base};
-    t.b = Operand{maps[c.b_map], c.b_mn, c.b_mn_base + nt * BN, c.b_k_base};
+    t.a = Operand{map(c.a_map), c.a_mn, c.a_mn_base + mt * BM, c.a_k_base};
+    t.b = Operand{map(c.b_map), c.b_mn, c.b_mn_base + nt * BN, c.b_k_base};
     t.kblocks = c.kblocks;
     return t;
   }
@@ -208,7 +221,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
                 const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
                 const __grid_constant__ CUtensorMap m4, const __grid_constant__ CUtensorMap m5, GemmSched sched,
-                int32_t* status) {
+                int* counter, int32_t* status) {
   sched.maps[0] = &m0;
   sched.maps[1] = &m1;
   sched.maps[2] = &m2;
@@ -218,17 +231,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 6; ++i) tma_prefetch_desc(sched.maps[i]);
   }
-  run_cta(sched, status, [&](uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
+  const Feed feed{counter, sched.num_units()};
+  run_cta(sched, feed, status, [&](uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
     const int q = warp & 3;
     uint8_t* stage_ptr = smem + SMEM_STAGING_OFF + (warp - 2) * STAGING_PER_WARP;
     const uint32_t staging = smem_u32(stage_ptr);
     uint32_t tcount = 0, nstore = 0;
-    const int nu = sched.num_units();
-    for (int u = blockIdx.x; u < nu; u += gridDim.x, ++tcount) {
+    for (uint32_t i = 0;; ++i, ++tcount) {
+      const int u = feed_consume(feed, ctl, i, status, true);
+      if (u < 0) break;
       int k, mt, nt;
       sched.decode(u, k, mt, nt);
       const GemmClass& c = sched.cls[k];
-      const CUtensorMap* out = sched.maps[c.out_map];
+      const CUtensorMap* out = sched.map(c.out_map);
       const int orow = c.out_row_base + mt * BM + 32 * q;
       const int ocol0 = c.out_col_base + nt * BN;
       uint32_t taddr;
@@ -315,7 +330,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
   }
   prof_begin(kind, st);
   gemm_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.maps[0], L.maps[1], L.maps[2], L.maps[3], L.maps[4],
-                                                       L.maps[5], sched, L.status);
+                                                       L.maps[5], sched, L.counter, L.status);
   prof_end(kind, st);
   return cudaGetLastError();
 }

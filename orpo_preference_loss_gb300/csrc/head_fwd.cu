@@ -111,15 +111,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&mh);
     tma_prefetch_desc(&mw);
   }
-  run_cta(sched, p.status, [&](uint8_t*, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
+  const Feed feed{nullptr, sched.num_units()};
+  run_cta(sched, feed, p.status, [&](uint8_t*, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
     const int q = warp & 3;
     const bool cap = p.softcap > 0.f;
     const float K = cap ? 2.f * kLog2e / p.softcap : 0.f;
     const float A = cap ? p.softcap * kLog2e : 0.f;
     const float B2 = 2.f * A;
     uint32_t tcount = 0;
-    const int nu = sched.num_units();
-    for (int u = blockIdx.x; u < nu; u += gridDim.x) {
+    for (uint32_t i = 0;; ++i) {
+      const int u = feed_consume(feed, ctl, i, p.status, true);
+      if (u < 0) break;
       const int s = u / sched.n_mt, mt = u - s * sched.n_mt;
       const int row = mt * BM + 32 * q + lane;
       int y = -1;

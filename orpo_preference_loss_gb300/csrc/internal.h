@@ -63,6 +63,7 @@ struct GemmClassH {
 struct GemmLaunch {
   CUtensorMap maps[6];
   GemmClassH cls[2];
+  int* counter;  // zeroed unit counter (dynamic scheduling), or nullptr for static round-robin
   int32_t* status;
   int grid;
 };
@@ -75,5 +76,9 @@ cudaError_t launch_loss(const float* logp, const int32_t* seq_id, const uint8_t*
 // ---- tensor maps (driver entry point fetched through the runtime)
 bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// MN-major bf16 operand [K, MN] (MN contiguous, MN % 64 == 0) viewed as {64, K, MN/64}: one TMA box
+// {64, 64, chunks} fetches `chunks` 64-wide column blocks of 64 k-rows, laid out block after block.
+bool encode_map_mn3d(CUtensorMap* map, const void* base, uint64_t mn, uint64_t k, uint64_t row_bytes,
+                     uint32_t chunks);
 
 }  // namespace orpo
