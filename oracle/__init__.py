@@ -15,5 +15,7 @@ from .orpo_oracle import (  # noqa: F401
     orpo_loss,
     head_backward,
     full_chain,
+    pref_loss,
+    PREF_KINDS,
     OracleError,
 )

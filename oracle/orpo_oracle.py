@@ -21,6 +21,10 @@ segmented backward)" page, and the "Steel flash-CCE — handoff" page):
   ``loss.ts`` bullet); metrics loss / nll / or / accuracy (``l_w > l_r``) /
   margin (mean chosen-minus-rejected log-odds, "Small sets over-fit fast").
   NLL scope is the ``response`` reading (``NLL = -l_w``).
+* ``pref_loss``     — the sibling objectives on the same logp engine ("Training
+  — design" §8.3 SimPO; the xtrain post-training page, Stage P1, for DPO's
+  summed sequence log-prob with cached reference log-probs; IPO and hinge are
+  named there without formulas and take their standard forms).
 * ``head_backward`` — implementation spec, backward bullet: recompute the
   logits, ``dZ = g * (onehot_y - softmax(z~)) * sech^2(z / c)``, then
   ``dh = dZ W`` and (the head-weight gradient that the pages leave to the
@@ -275,3 +279,90 @@ def full_chain(h, W, targets, mask, seq_id, n_pairs, lam, softcap=0.0):
     res = orpo_loss(logp, seq_id, mask, n_pairs, lam)
     dh, dW = head_backward(h, W, targets, mask, lse, res.g, softcap)
     return logp, lse, res, dh, dW
+
+
+# --------------------------------------------------------------------------
+# sibling preference objectives on the same per-token logp
+# --------------------------------------------------------------------------
+
+PREF_KINDS = ("orpo", "simpo", "dpo", "ipo", "hinge")
+
+
+def pref_loss(kind: str, logp, seq_id, mask, n_pairs: int, beta: float, gamma: float = 0.0, ref=None):
+    """Preference objective `kind` over pairs, value and gradient w.r.t. each logp.
+
+    orpo  : the ORPO objective above with lambda = beta (gamma unused).
+    simpo : mean response log-prob l; per pair softplus(-beta((l_w - l_r) - gamma))
+            ("Training — design" §8.3); no NLL term.
+    dpo   : per-sequence SUM s of logp over response rows, cached reference sums
+            r (ref[2P]); D = (s_w - r_w) - (s_r - r_r); per pair
+            -log sigmoid(beta * D) (xtrain post-training page, Stage P1).
+    ipo   : (D - 1/(2 beta))^2 on the same D (the standard IPO loss; the pages
+            only name it).
+    hinge : max(0, 1 - beta * D) (SLiC-style hinge on the same D; named only).
+    The batch value is the mean over pairs.  Returns a LossResult whose `ell`
+    holds the per-sequence mean (orpo, simpo) or sum (dpo, ipo, hinge), `nll`
+    is mean(-ell_w), `orr` the mean preference term, `accuracy` the fraction of
+    pairs whose chosen statistic (ell_w, or s_w - r_w) beats the rejected one,
+    and `margin` the mean of the argument the preference term is applied to.
+    """
+    if kind == "orpo":
+        return orpo_loss(logp, seq_id, mask, n_pairs, beta)
+    if kind not in PREF_KINDS:
+        raise OracleError("arg", f"unknown kind {kind}")
+    logp = np.asarray(logp, dtype=np.float64)
+    seq_id = np.asarray(seq_id).astype(np.int64)
+    mask = np.asarray(mask).astype(bool)
+    P = int(n_pairs)
+    S = 2 * P
+    if P < 1:
+        raise OracleError("arg", "n_pairs must be >= 1")
+    if np.any((seq_id < -1) | (seq_id >= S)) or np.any(np.diff(seq_id[seq_id >= 0]) < 0):
+        raise OracleError("seqid", "bad sequence ids")
+    use = (seq_id >= 0) & mask
+    n = np.bincount(seq_id[use], minlength=S).astype(np.float64)
+    if np.any(n == 0):
+        raise OracleError("empty", "a sequence has no response token")
+    tot = np.bincount(seq_id[use], weights=logp[use], minlength=S)
+    mean_kind = kind == "simpo"
+    ell = tot / n if mean_kind else tot
+    w, r = ell[0::2], ell[1::2]
+    if mean_kind:
+        u = beta * ((w - r) - gamma)
+        term = softplus(-u)
+        dterm_dw = -beta * sigmoid(-u)             # d term / d l_w ; d / d l_r is the negative
+        chosen_better = w > r
+        margin = u
+    else:
+        if ref is None:
+            raise OracleError("arg", "reference log-probs are required")
+        ref = np.asarray(ref, dtype=np.float64)
+        D = (w - ref[0::2]) - (r - ref[1::2])
+        chosen_better = D > 0
+        if kind == "dpo":
+            term = softplus(-beta * D)
+            dterm_dw = -beta * sigmoid(-beta * D)
+            margin = beta * D
+        elif kind == "ipo":
+            if beta <= 0:
+                raise OracleError("arg", "ipo needs beta > 0")
+            c = D - 1.0 / (2.0 * beta)
+            term = c * c
+            dterm_dw = 2.0 * c
+            margin = D
+        else:  # hinge
+            a = 1.0 - beta * D
+            term = np.maximum(a, 0.0)
+            dterm_dw = np.where(a > 0, -beta, 0.0)
+            margin = beta * D
+    G = np.empty(S)
+    G[0::2] = dterm_dw / P
+    G[1::2] = -dterm_dw / P
+    g = np.zeros_like(logp)
+    scale = n[seq_id[use]] if mean_kind else 1.0
+    g[use] = G[seq_id[use]] / scale
+    loss = float(np.mean(term))
+    if not np.isfinite(loss):
+        raise OracleError("nonfinite", "loss is not finite")
+    return LossResult(loss=loss, nll=float(np.mean(-w)), orr=loss, accuracy=float(np.mean(chosen_better)),
+                      margin=float(np.mean(margin)), ell=ell, log_odds=margin, g=g, n=n)
