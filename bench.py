@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--loss", default="orpo", choices=["orpo", "simpo", "dpo", "ipo", "hinge"],
+                    help="preference objective between forward and backward (orpo_loss for orpo)")
     ap.add_argument("--M", type=int, default=None, help="shrink the workload's rows (profiling cases)")
     ap.add_argument("--V", type=int, default=None, help="shrink the vocabulary (profiling cases)")
     ap.add_argument("--d", type=int, default=None, help="change the hidden size (profiling cases)")
@@ -75,15 +77,20 @@ def workload_config(w):
             "l2": "inputs larger than L2 (W alone is %.2f GB)" % (w.V * w.d * 2 / 1e9)}
 
 
-def kernel_sources_sha():
-    import glob
+# device code each kernel kind is built from (its DRAM-traffic figure is void once any of these changes)
+KERNEL_SOURCES = {
+    "fwd_logits": ("head_fwd.cu", "engine.cuh", "ptx.cuh"),
+    "bwd_recompute": ("head_bwd.cu", "engine.cuh", "ptx.cuh"),
+    "bwd_grad_gemm": ("head_bwd.cu", "engine.cuh", "ptx.cuh"),
+}
+
+
+def kernel_sources_sha(kernel):
     import hashlib
     c = os.path.join(ROOT, "orpo_preference_loss_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(c, "*.cu"))) + sorted(glob.glob(os.path.join(c, "*.cuh"))) + \
-        sorted(glob.glob(os.path.join(c, "*.h")))
     h = hashlib.sha256()
-    for f in files:
-        with open(f, "rb") as fh:
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(c, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -100,7 +107,7 @@ def profiled_traffic(w, kernel):
     for line in text.splitlines():
         if line.startswith("traffic_bytes_per_launch"):
             fields = dict(kv.split("=") for kv in line.split()[1:])
-            if fields.get("sources") != kernel_sources_sha():
+            if kernel not in KERNEL_SOURCES or fields.get("sources_" + kernel) != kernel_sources_sha(kernel):
                 return None
             v = fields.get(kernel)
             return int(v) if v is not None else None
@@ -248,6 +255,10 @@ def ours(args, w, rank, world, local):
     dh = torch.empty((M, d), dtype=torch.float32, device=dev)
     dW = torch.empty((V, d), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # cached reference sums for the DPO-family objectives: seeded synthetic values per sequence
+    ref = torch.from_numpy((-6.0 * np.bincount(np.maximum(w.seq_id, 0), minlength=2 * P)[:2 * P]
+                            + np.random.default_rng(17).standard_normal(2 * P)).astype(np.float32)).to(dev)
+    beta = {"orpo": w.lam, "simpo": 2.0, "dpo": 0.1, "ipo": 0.1, "hinge": 0.1}[args.loss]
     torch.cuda.synchronize()
     mem_before = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)
@@ -255,7 +266,10 @@ def ours(args, w, rank, world, local):
 
     def step():
         orpo.orpo_head_fwd(h_bf, W_bf, t["targets"], t["mask"], w.softcap, logp, lse, ws, status)
-        orpo.orpo_loss(logp, t["seq_id"], t["mask"], P, w.lam, out, ell, g, status)
+        if args.loss == "orpo":
+            orpo.orpo_loss(logp, t["seq_id"], t["mask"], P, w.lam, out, ell, g, status)
+        else:
+            orpo.orpo_pref_loss(args.loss, logp, t["seq_id"], t["mask"], P, beta, 0.5, ref, out, ell, g, status)
         orpo.orpo_head_bwd(h_bf, W_bf, t["targets"], t["mask"], lse, g, w.softcap, dh, dW, False, ws, status)
 
     for _ in range(args.warmup):
@@ -349,7 +363,8 @@ def ours(args, w, rank, world, local):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+            "config": dict(workload_config(w), objective=args.loss,
+                           parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
             "tflops": tflops, "frac_of_peak": tflops / sustained, "frac_of_burst_peak": tflops / burst,
             "peak_extra_gb": peak_extra / 1e9, "e2e": e2e, "gpu_launches": sum(v["launches"] for v in
                                                                                kernels.values()),

@@ -128,6 +128,30 @@ int orpo_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int
               int32_t* status, void* stream);
 
 /*
+ * Sibling preference objectives on the same per-token logp (design page §8.3
+ * "Objective variants": SimPO, IPO, hinge/SLiC; the xtrain post-training page,
+ * Stage P1, for DPO with cached reference log-probs).  Same layouts, status
+ * bits, determinism and limits as orpo_loss; only the per-pair term differs.
+ * Per sequence the statistic is the mean of logp over its response rows
+ * (ORPO, SimPO) or the sum (DPO, IPO, hinge), written to ell[2P].  With
+ * D = (s_w - ref_logp[2p]) - (s_r - ref_logp[2p+1]) (ref_logp: device fp32
+ * [2P], per-sequence reference sums; required for DPO, IPO, hinge):
+ *   ORPO_PREF_ORPO  : exactly orpo_loss with lambda = beta (gamma unused)
+ *   ORPO_PREF_SIMPO : softplus(-beta((l_w - l_r) - gamma))
+ *   ORPO_PREF_DPO   : -log sigmoid(beta D)
+ *   ORPO_PREF_IPO   : (D - 1/(2 beta))^2            (beta > 0)
+ *   ORPO_PREF_HINGE : max(0, 1 - beta D)
+ * loss = mean over pairs; out[0..4] = loss, mean(-statistic_w), mean preference
+ * term, accuracy (chosen statistic beats rejected: l_w > l_r, or D > 0), margin
+ * (mean of the argument of the term: x, beta((l_w-l_r)-gamma), beta D, D, beta D).
+ * g[t] = d loss / d logp[t]: G_s / n_s for the mean kinds, G_s for the sum kinds.
+ */
+enum { ORPO_PREF_ORPO = 0, ORPO_PREF_SIMPO = 1, ORPO_PREF_DPO = 2, ORPO_PREF_IPO = 3, ORPO_PREF_HINGE = 4 };
+int orpo_pref_loss(int kind, const float* logp, const int32_t* seq_id, const uint8_t* mask, int64_t M,
+                   int32_t n_pairs, float beta, float gamma, const float* ref_logp, float* out, float* ell,
+                   float* g, int32_t* status, void* stream);
+
+/*
  * Backward of the head (fused-head spec, backward bullet; steel handoff,
  * backward structure).  With p = exp(z~ - lse) rebuilt from the saved lse and
  * the logits recomputed tile by tile:
@@ -188,6 +212,15 @@ int orpo_debug_gemm(const void* A_bf16, const void* B_bf16, float* C, int64_t M,
 int orpo_head_fwd_static(const void* h_bf16, const void* W_bf16, const int32_t* targets,
                          const uint8_t* mask, int64_t M, int64_t V, int64_t d, float softcap,
                          float* logp, float* lse, int32_t* status, void* stream);
+
+/*
+ * Diagnostic: failure detection without a fault (no counterpart on the pages).
+ * Launches one thread that waits, through the same bounded wait every pipeline
+ * role of the library uses, on a shared-memory barrier that nothing completes.
+ * After limit_ns (1 us .. 2 s) the wait gives up, ORPO_STATUS_TIMEOUT is OR-ed
+ * into *status (device word) and the kernel returns; the context stays usable.
+ */
+int orpo_debug_wait_timeout(int32_t* status, int64_t limit_ns, void* stream);
 
 /*
  * Diagnostic: device time of the library's own launches (no counterpart on

@@ -19,7 +19,8 @@ from . import build as _build
 __all__ = [
     "OrpoError", "load", "lib_path", "orpo_head_workspace_bytes", "orpo_head_fwd", "orpo_loss",
     "orpo_head_bwd", "orpo_status_string", "orpo_debug_gemm", "OrpoHead", "STATUS_BITS",
-    "orpo_profile_start", "orpo_profile_stop", "orpo_head_fwd_static",
+    "orpo_profile_start", "orpo_profile_stop", "orpo_head_fwd_static", "orpo_debug_wait_timeout",
+    "orpo_pref_loss", "PREF_KINDS",
 ]
 
 STATUS_BITS = {"target": 1 << 4, "seqid": 1 << 5, "empty": 1 << 6, "nonfinite": 1 << 7, "timeout": 1 << 8}
@@ -60,8 +61,12 @@ def load():
     L.orpo_status_string.restype = ctypes.c_char_p
     L.orpo_debug_gemm.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, vp]
     L.orpo_debug_gemm.restype = ctypes.c_int
+    L.orpo_pref_loss.argtypes = [ctypes.c_int, vp, vp, vp, i64, i32, f32, f32, vp, vp, vp, vp, vp, vp]
+    L.orpo_pref_loss.restype = ctypes.c_int
     L.orpo_head_fwd_static.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp, vp, vp, vp]
     L.orpo_head_fwd_static.restype = ctypes.c_int
+    L.orpo_debug_wait_timeout.argtypes = [vp, i64, vp]
+    L.orpo_debug_wait_timeout.restype = ctypes.c_int
     L.orpo_profile_start.argtypes = []
     L.orpo_profile_start.restype = ctypes.c_int
     L.orpo_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), ctypes.c_int]
@@ -161,6 +166,27 @@ def orpo_loss(logp, seq_id, mask, n_pairs, lam, out, ell, g, status, stream=None
                             _ptr(ell), _ptr(g), _ptr(status), _stream(stream)), "orpo_loss")
 
 
+PREF_KINDS = {"orpo": 0, "simpo": 1, "dpo": 2, "ipo": 3, "hinge": 4}
+
+
+def orpo_pref_loss(kind, logp, seq_id, mask, n_pairs, beta, gamma, ref_logp, out, ell, g, status, stream=None):
+    """Sibling preference objective `kind` (orpo, simpo, dpo, ipo, hinge) on per-token logp."""
+    M = logp.shape[0]
+    k = PREF_KINDS[kind] if isinstance(kind, str) else int(kind)
+    _dev(logp, "logp", (torch.float32,), (M,))
+    _dev(seq_id, "seq_id", (torch.int32,), (M,))
+    _dev(mask, "mask", (torch.uint8, torch.bool), (M,))
+    _dev(out, "out", (torch.float32,), (5,))
+    _dev(ell, "ell", (torch.float32,), (2 * n_pairs,))
+    _dev(g, "g", (torch.float32,), (M,))
+    _dev(status, "status", (torch.int32,))
+    if ref_logp is not None:
+        _dev(ref_logp, "ref_logp", (torch.float32,), (2 * n_pairs,))
+    _check(load().orpo_pref_loss(k, _ptr(logp), _ptr(seq_id), _ptr(mask), M, int(n_pairs), float(beta), float(gamma),
+                                 _ptr(ref_logp), _ptr(out), _ptr(ell), _ptr(g), _ptr(status), _stream(stream)),
+           "orpo_pref_loss")
+
+
 def orpo_head_bwd(h, W, targets, mask, lse, g, softcap, dh, dW, accumulate_dW, workspace, status,
                   stream=None):
     M, d = h.shape
@@ -186,6 +212,11 @@ def orpo_debug_gemm(A, B, C, M, N, K, a_mn_major, b_mn_major, status, stream=Non
     _dev(C, "C", (torch.float32,), (M, N))
     _check(load().orpo_debug_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(a_mn_major), int(b_mn_major),
                                   _ptr(status), _stream(stream)), "orpo_debug_gemm")
+
+
+def orpo_debug_wait_timeout(status, limit_ns, stream=None):
+    _dev(status, "status", (torch.int32,))
+    _check(load().orpo_debug_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)), "orpo_debug_wait_timeout")
 
 
 PROFILE_KINDS = 6

@@ -207,7 +207,27 @@ int orpo_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int
   int sms = 0;
   if (int e = device_check(&sms)) return e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return launch_loss(logp, seq_id, mask, (int)M, n_pairs, lambda, out, ell, g, status, st) == cudaSuccess
+  return launch_loss(ORPO_PREF_ORPO, logp, seq_id, mask, (int)M, n_pairs, lambda, 0.f, nullptr, out, ell, g, status,
+                     st) == cudaSuccess
+             ? ORPO_OK
+             : ORPO_ERR_CUDA;
+}
+
+int orpo_pref_loss(int kind, const float* logp, const int32_t* seq_id, const uint8_t* mask, int64_t M,
+                   int32_t n_pairs, float beta, float gamma, const float* ref_logp, float* out, float* ell, float* g,
+                   int32_t* status, void* stream) {
+  if (kind < ORPO_PREF_ORPO || kind > ORPO_PREF_HINGE) return ORPO_ERR_ARG;
+  if (M < 0 || M > kMaxRows || n_pairs < 1 || n_pairs > ORPO_MAX_PAIRS) return ORPO_ERR_SHAPE;
+  const bool needs_ref = kind == ORPO_PREF_DPO || kind == ORPO_PREF_IPO || kind == ORPO_PREF_HINGE;
+  if (!out || !ell || !status || (M > 0 && (!logp || !seq_id || !mask || !g)) || (needs_ref && !ref_logp))
+    return ORPO_ERR_NULL;
+  if (!isfinite(beta) || beta < 0.f || !isfinite(gamma) || (kind == ORPO_PREF_IPO && !(beta > 0.f)))
+    return ORPO_ERR_ARG;
+  int sms = 0;
+  if (int e = device_check(&sms)) return e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return launch_loss(kind, logp, seq_id, mask, (int)M, n_pairs, beta, gamma, needs_ref ? ref_logp : nullptr, out,
+                     ell, g, status, st) == cudaSuccess
              ? ORPO_OK
              : ORPO_ERR_CUDA;
 }

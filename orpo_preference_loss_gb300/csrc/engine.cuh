@@ -68,7 +68,8 @@ struct Feed {
   int nu;
 };
 
-__device__ __forceinline__ bool wait_phase(SmemCtl* ctl, uint64_t* bar, uint32_t parity, int32_t* status);
+__device__ __forceinline__ bool wait_phase(SmemCtl* ctl, uint64_t* bar, uint32_t parity, int32_t* status,
+                                           uint64_t limit_ns = kWaitLimitNs);
 
 // Producer side: returns the next unit, -1 when done, -2 on abort.
 __device__ __forceinline__ int feed_produce(const Feed& f, SmemCtl* ctl, uint32_t i, int32_t* status) {
@@ -128,14 +129,15 @@ __device__ __forceinline__ uint8_t* smem_base_aligned() {
 }
 
 // Bounded wait on an mbarrier phase.  Returns false on abort / timeout.
-__device__ __forceinline__ bool wait_phase(SmemCtl* ctl, uint64_t* bar, uint32_t parity, int32_t* status) {
+__device__ __forceinline__ bool wait_phase(SmemCtl* ctl, uint64_t* bar, uint32_t parity, int32_t* status,
+                                           uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (ctl->abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         atomicOr(status, kStatusTimeout);
         ctl->abort_flag = 1;
         return false;

@@ -70,8 +70,10 @@ struct GemmLaunch {
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind);
 
 // ---- loss
-cudaError_t launch_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int M, int P, float lam,
-                        float* out, float* ell, float* g, int32_t* status, cudaStream_t st);
+// kind: 0 ORPO (beta = lambda), 1 SimPO, 2 DPO, 3 IPO, 4 hinge; ref = per-sequence reference sums or nullptr
+cudaError_t launch_loss(int kind, const float* logp, const int32_t* seq_id, const uint8_t* mask, int M, int P,
+                        float beta, float gamma, const float* ref, float* out, float* ell, float* g, int32_t* status,
+                        cudaStream_t st);
 
 // ---- tensor maps (driver entry point fetched through the runtime)
 bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,

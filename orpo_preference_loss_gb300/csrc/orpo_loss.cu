@@ -13,6 +13,12 @@
 // first and last runs of each chunk are partial and are combined per sequence
 // by one warp in a fixed lane/butterfly order, so the result is bitwise
 // reproducible.  Per-pair arithmetic is fp64; outputs are fp32.
+//
+// The same kernel evaluates the sibling objectives that share the logp engine
+// ("Training — design" §8.3 SimPO; the xtrain post-training page's DPO with a
+// summed sequence log-prob and cached reference log-probs; IPO and a hinge on
+// the same reference log-ratio): only the per-pair term and its derivative
+// change, and whether a sequence is summarised by its mean or its sum.
 #include <math.h>
 
 #include "internal.h"
@@ -22,6 +28,7 @@ namespace orpo {
 namespace {
 
 constexpr int T = 1024;
+constexpr int kKindOrpo = 0, kKindSimpo = 1, kKindDpo = 2, kKindIpo = 3, kKindHinge = 4;
 constexpr int32_t kSeqErr = 1 << 5, kEmptyErr = 1 << 6, kNonfiniteErr = 1 << 7;
 
 struct LossSmem {
@@ -46,9 +53,10 @@ __device__ __forceinline__ double sigmoid_d(double x) {
 }
 
 __global__ void __launch_bounds__(T, 1)
-    loss_kernel(const float* __restrict__ logp, const int32_t* __restrict__ seq_id,
-                const uint8_t* __restrict__ mask, int M, int P, float lam_f, float* __restrict__ out,
-                float* __restrict__ ell, float* __restrict__ g, int32_t* status) {
+    loss_kernel(int kind, const float* __restrict__ logp, const int32_t* __restrict__ seq_id,
+                const uint8_t* __restrict__ mask, int M, int P, float lam_f, float gamma_f,
+                const float* __restrict__ ref, float* __restrict__ out, float* __restrict__ ell,
+                float* __restrict__ g, int32_t* status) {
   extern __shared__ __align__(16) uint8_t raw[];
   LossSmem& sm = *reinterpret_cast<LossSmem*>(raw);
   const int S = 2 * P;
@@ -56,7 +64,9 @@ __global__ void __launch_bounds__(T, 1)
   int* seq_cnt = reinterpret_cast<int*>(seq_sum + S);
   double* G = reinterpret_cast<double*>(raw + sizeof(LossSmem) + (size_t)S * 8 + (((size_t)S * 4 + 7) & ~size_t(7)));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const double lam = (double)lam_f;
+  const double lam = (double)lam_f;  // lambda for ORPO, beta for the other kinds
+  const double gam = (double)gamma_f;
+  const bool mean_kind = kind == kKindOrpo || kind == kKindSimpo;
 
   if (tid == 0) sm.err = 0;
   for (int s = tid; s < S; s += T) {
@@ -158,39 +168,75 @@ __global__ void __launch_bounds__(T, 1)
   }
   __syncthreads();
 
-  // ---- phase 3: per-sequence means
+  // ---- phase 3: per-sequence statistic: mean (ORPO, SimPO) or sum (DPO, IPO, hinge)
   for (int s = tid; s < S; s += T) {
     const int n = seq_cnt[s];
     double l = NAN;
     if (n == 0)
       err |= kEmptyErr;
     else
-      l = seq_sum[s] / (double)n;
+      l = mean_kind ? seq_sum[s] / (double)n : seq_sum[s];
     seq_sum[s] = l;
     ell[s] = (float)l;
   }
   __syncthreads();
 
-  // ---- phase 4: per pair value, metrics and gradient
+  // ---- phase 4: per pair value, metrics and gradient (G = d loss / d statistic)
   double c_loss = 0.0, c_nll = 0.0, c_or = 0.0, c_acc = 0.0, c_mar = 0.0;
   for (int p = tid; p < P; p += T) {
     const double lw = seq_sum[2 * p], lr = seq_sum[2 * p + 1];
-    const double x = (lw - lr) - (log1mexp_d(lw) - log1mexp_d(lr));
-    const double lor = softplus_d(-x);
-    const double sg = sigmoid_d(-x);
-    const double inv_w = -1.0 / expm1(lw), inv_r = -1.0 / expm1(lr);
-    const double Gw = (-1.0 - lam * sg * inv_w) / (double)P;
-    const double Gr = (lam * sg * inv_r) / (double)P;
-    if (lw > 0.0 || lr > 0.0 || !isfinite(x) || !isfinite(Gw) || !isfinite(Gr) || !isfinite(lor) ||
-        !isfinite(lw))
+    double term = 0.0, dw = 0.0, margin = 0.0, Gw, Gr, loss_p;
+    bool better;
+    if (kind == kKindOrpo) {
+      // x = (l_w - l_r) - (log1mexp(l_w) - log1mexp(l_r)); loss_p = -l_w + lambda softplus(-x)
+      const double x = (lw - lr) - (log1mexp_d(lw) - log1mexp_d(lr));
+      term = softplus_d(-x);
+      const double sg = sigmoid_d(-x);
+      const double inv_w = -1.0 / expm1(lw), inv_r = -1.0 / expm1(lr);  // 1 / (1 - e^l)
+      Gw = (-1.0 - lam * sg * inv_w) / (double)P;
+      Gr = (lam * sg * inv_r) / (double)P;
+      loss_p = -lw + lam * term;
+      margin = x;
+      better = lw > lr;
+      if (lw > 0.0 || lr > 0.0) err |= kNonfiniteErr;
+    } else {
+      if (kind == kKindSimpo) {
+        margin = lam * ((lw - lr) - gam);  // softplus(-beta((l_w - l_r) - gamma))
+        term = softplus_d(-margin);
+        dw = -lam * sigmoid_d(-margin);
+        better = lw > lr;
+      } else {
+        const double D = (lw - (double)ref[2 * p]) - (lr - (double)ref[2 * p + 1]);
+        better = D > 0.0;
+        if (kind == kKindDpo) {  // -log sigmoid(beta D)
+          margin = lam * D;
+          term = softplus_d(-margin);
+          dw = -lam * sigmoid_d(-margin);
+        } else if (kind == kKindIpo) {  // (D - 1/(2 beta))^2
+          const double c = D - 1.0 / (2.0 * lam);
+          margin = D;
+          term = c * c;
+          dw = 2.0 * c;
+        } else {  // hinge: max(0, 1 - beta D)
+          const double a = 1.0 - lam * D;
+          margin = lam * D;
+          term = a > 0.0 ? a : 0.0;
+          dw = a > 0.0 ? -lam : 0.0;
+        }
+      }
+      Gw = dw / (double)P;
+      Gr = -dw / (double)P;
+      loss_p = term;
+    }
+    if (!isfinite(term) || !isfinite(Gw) || !isfinite(Gr) || !isfinite(lw) || !isfinite(lr) || !isfinite(margin))
       err |= kNonfiniteErr;
     G[2 * p] = Gw;
     G[2 * p + 1] = Gr;
-    c_loss += -lw + lam * lor;
+    c_loss += loss_p;
     c_nll += -lw;
-    c_or += lor;
-    c_acc += lw > lr ? 1.0 : 0.0;
-    c_mar += x;
+    c_or += term;
+    c_acc += better ? 1.0 : 0.0;
+    c_mar += margin;
   }
   // fixed-order block reduction of the five sums
   double v[5] = {c_loss, c_nll, c_or, c_acc, c_mar};
@@ -219,7 +265,7 @@ __global__ void __launch_bounds__(T, 1)
     float gv = 0.f;
     if (sid >= 0 && sid < S && mask[t] != 0) {
       const int n = seq_cnt[sid];
-      if (n > 0) gv = (float)(G[sid] / (double)n);
+      if (n > 0) gv = (float)(mean_kind ? G[sid] / (double)n : G[sid]);
     }
     g[t] = gv;
   }
@@ -232,13 +278,14 @@ size_t loss_smem_bytes(int P) {
   return sizeof(LossSmem) + S * 8 + ((S * 4 + 7) & ~size_t(7)) + S * 8;
 }
 
-cudaError_t launch_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int M, int P, float lam,
-                        float* out, float* ell, float* g, int32_t* status, cudaStream_t st) {
+cudaError_t launch_loss(int kind, const float* logp, const int32_t* seq_id, const uint8_t* mask, int M, int P,
+                        float beta, float gamma, const float* ref, float* out, float* ell, float* g, int32_t* status,
+                        cudaStream_t st) {
   const size_t smem = loss_smem_bytes(P);
   cudaError_t e = cudaFuncSetAttribute(loss_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   prof_begin(K_LOSS, st);
-  loss_kernel<<<1, T, smem, st>>>(logp, seq_id, mask, M, P, lam, out, ell, g, status);
+  loss_kernel<<<1, T, smem, st>>>(kind, logp, seq_id, mask, M, P, beta, gamma, ref, out, ell, g, status);
   prof_end(K_LOSS, st);
   return cudaGetLastError();
 }
