@@ -109,6 +109,15 @@ def softcap_slope(z: np.ndarray, c: float) -> np.ndarray:
     return np.ones_like(z)
 
 
+PROMPT = 2  # mask value of a prompt row that only the full-scope NLL supervises
+
+
+def _response_rows(mask) -> np.ndarray:
+    """Response rows: nonzero mask other than the prompt marker."""
+    m = np.asarray(mask)
+    return (m != 0) & (m != PROMPT)
+
+
 def _row_chunk(V: int, budget_elems: int = 1 << 23) -> int:
     return max(1, budget_elems // max(1, V))
 
@@ -170,22 +179,29 @@ class LossResult:
 
 
 def orpo_loss(logp: np.ndarray, seq_id: np.ndarray, mask: np.ndarray, n_pairs: int,
-              lam: float) -> LossResult:
+              lam: float, scope: str = "response") -> LossResult:
     """ORPO objective and its gradient with respect to every per-token logp.
 
     Sequence 2p is the chosen response of pair p and 2p+1 the rejected one.
-    Rows with seq_id = -1 are padding.  l_s is the mean of logp over the
-    mask = 1 rows of sequence s.  Per pair:
+    Rows with seq_id = -1 are padding.  mask: 0 = not supervised, 2 = prompt
+    row (only the full-scope NLL sees it), any other nonzero value = response
+    row.  l_s is the mean of logp over the response rows of sequence s.  Per pair:
         x_p  = (l_w - l_r) - (log1mexp(l_w) - log1mexp(l_r))
-        L    = (1/P) sum_p [ -l_w + lam * softplus(-x_p) ]
+        L    = (1/P) sum_p [ NLL_p + lam * softplus(-x_p) ]
+    with NLL_p = -l_w (scope "response"), or, for scope "full" ("Training —
+    design" §1, combineFullNll), the token mean of -logp over the chosen
+    sequence's prompt and response rows: -((P-1) pm + M l_w) / ((P-1) + M).
     Gradient (closed form; d x / d l_w = 1 / (1 - e^{l_w})):
-        G_w = (1/P) (-1 - lam * sigmoid(-x) / (1 - e^{l_w}))
-        G_r = (1/P) ( lam * sigmoid(-x) / (1 - e^{l_r}))
-        g_t = mask_t * G_{s(t)} / n_{s(t)}
+        OR part: G_w = -(lam/P) sigmoid(-x) / (1 - e^{l_w}),
+                 G_r =  (lam/P) sigmoid(-x) / (1 - e^{l_r}),  spread as G_s / n_s
+                 over the response rows of s;
+        NLL part: -1/(P n_w) on the chosen response rows (response scope), or
+                 -1/(P N_w) on every chosen prompt and response row (full scope).
     """
+    if scope not in ("response", "full"):
+        raise OracleError("arg", "scope is 'response' or 'full'")
     logp = np.asarray(logp, dtype=np.float64)
     seq_id = np.asarray(seq_id).astype(np.int64)
-    mask = np.asarray(mask).astype(bool)
     P = int(n_pairs)
     if P < 1:
         raise OracleError("arg", "n_pairs must be >= 1")
@@ -196,7 +212,8 @@ def orpo_loss(logp: np.ndarray, seq_id: np.ndarray, mask: np.ndarray, n_pairs: i
     ids = seq_id[valid]
     if np.any(np.diff(ids) < 0):
         raise OracleError("seqid", "sequence ids are not non-decreasing")
-    use = valid & mask
+    use = valid & _response_rows(mask)
+    sup = valid & (np.asarray(mask) != 0)          # response + prompt rows (full-scope NLL)
     n = np.bincount(seq_id[use], minlength=S).astype(np.float64)
     if np.any(n == 0):
         raise OracleError("empty", f"sequence {int(np.argmin(n))} has no response token")
@@ -205,10 +222,13 @@ def orpo_loss(logp: np.ndarray, seq_id: np.ndarray, mask: np.ndarray, n_pairs: i
     lw, lr = ell[0::2], ell[1::2]
     if np.any(ell > 0):
         raise OracleError("nonfinite", "a mean log-prob is positive")
+    N = np.bincount(seq_id[sup], minlength=S).astype(np.float64)
+    tot_full = np.bincount(seq_id[sup], weights=logp[sup], minlength=S)
+    nll_p = -lw if scope == "response" else -(tot_full[0::2] / N[0::2])
     with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
         x = (lw - lr) - (log1mexp(lw) - log1mexp(lr))
         lor = softplus(-x)
-        nll = float(np.mean(-lw))
+        nll = float(np.mean(nll_p))
         orr = float(np.mean(lor))
         loss = nll + lam * orr
         acc = float(np.mean(lw > lr))
@@ -217,7 +237,7 @@ def orpo_loss(logp: np.ndarray, seq_id: np.ndarray, mask: np.ndarray, n_pairs: i
         # 1 / (1 - e^l) = -1 / expm1(l)
         inv_w = -1.0 / np.expm1(lw)
         inv_r = -1.0 / np.expm1(lr)
-        Gw = (-1.0 - lam * sig * inv_w) / P
+        Gw = (-lam * sig * inv_w) / P
         Gr = (lam * sig * inv_r) / P
     # l = 0 (a response whose every target has probability 1) makes log1mexp
     # -inf; the value and gradient are then reported as non-finite, not clamped.
@@ -228,6 +248,13 @@ def orpo_loss(logp: np.ndarray, seq_id: np.ndarray, mask: np.ndarray, n_pairs: i
     G[0::2], G[1::2] = Gw, Gr
     g = np.zeros_like(logp)
     g[use] = G[seq_id[use]] / n[seq_id[use]]
+    chosen = (seq_id % 2 == 0)
+    if scope == "response":
+        rows = use & chosen
+        g[rows] += -1.0 / (P * n[seq_id[rows]])
+    else:
+        rows = sup & chosen
+        g[rows] += -1.0 / (P * N[seq_id[rows]])
     return LossResult(loss=loss, nll=nll, orr=orr, accuracy=acc, margin=margin,
                       ell=ell, log_odds=x, g=g, n=n)
 
@@ -273,10 +300,10 @@ def head_backward(h: np.ndarray, W: np.ndarray, targets: np.ndarray, mask: np.nd
     return dh, dW
 
 
-def full_chain(h, W, targets, mask, seq_id, n_pairs, lam, softcap=0.0):
+def full_chain(h, W, targets, mask, seq_id, n_pairs, lam, softcap=0.0, scope="response"):
     """Forward, loss and backward in sequence, as one training step of the head."""
     logp, lse = head_forward(h, W, targets, mask, softcap)
-    res = orpo_loss(logp, seq_id, mask, n_pairs, lam)
+    res = orpo_loss(logp, seq_id, mask, n_pairs, lam, scope)
     dh, dW = head_backward(h, W, targets, mask, lse, res.g, softcap)
     return logp, lse, res, dh, dW
 
@@ -312,14 +339,13 @@ def pref_loss(kind: str, logp, seq_id, mask, n_pairs: int, beta: float, gamma: f
         raise OracleError("arg", f"unknown kind {kind}")
     logp = np.asarray(logp, dtype=np.float64)
     seq_id = np.asarray(seq_id).astype(np.int64)
-    mask = np.asarray(mask).astype(bool)
     P = int(n_pairs)
     S = 2 * P
     if P < 1:
         raise OracleError("arg", "n_pairs must be >= 1")
     if np.any((seq_id < -1) | (seq_id >= S)) or np.any(np.diff(seq_id[seq_id >= 0]) < 0):
         raise OracleError("seqid", "bad sequence ids")
-    use = (seq_id >= 0) & mask
+    use = (seq_id >= 0) & _response_rows(mask)
     n = np.bincount(seq_id[use], minlength=S).astype(np.float64)
     if np.any(n == 0):
         raise OracleError("empty", "a sequence has no response token")
