@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--loss", default="orpo", choices=["orpo", "simpo", "dpo", "ipo", "hinge"],
+    ap.add_argument("--loss", default="orpo", choices=["orpo", "simpo", "dpo", "ipo", "hinge", "orpo_full"],
                     help="preference objective between forward and backward (orpo_loss for orpo)")
     ap.add_argument("--M", type=int, default=None, help="shrink the workload's rows (profiling cases)")
     ap.add_argument("--V", type=int, default=None, help="shrink the vocabulary (profiling cases)")
@@ -258,7 +258,7 @@ def ours(args, w, rank, world, local):
     # cached reference sums for the DPO-family objectives: seeded synthetic values per sequence
     ref = torch.from_numpy((-6.0 * np.bincount(np.maximum(w.seq_id, 0), minlength=2 * P)[:2 * P]
                             + np.random.default_rng(17).standard_normal(2 * P)).astype(np.float32)).to(dev)
-    beta = {"orpo": w.lam, "simpo": 2.0, "dpo": 0.1, "ipo": 0.1, "hinge": 0.1}[args.loss]
+    beta = {"orpo": w.lam, "simpo": 2.0, "dpo": 0.1, "ipo": 0.1, "hinge": 0.1, "orpo_full": w.lam}[args.loss]
     torch.cuda.synchronize()
     mem_before = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)

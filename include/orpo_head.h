@@ -110,7 +110,9 @@ int orpo_head_fwd(const void* h_bf16, const void* W_bf16, const int32_t* targets
  * Sequence 2p is the chosen response of pair p, sequence 2p+1 the rejected one.
  *   seq_id: int32 [M], -1 = padding row, else in [0, 2P); the ids that are not
  *           -1 must be non-decreasing in row order (padding may sit anywhere).
- *   l_s  = mean of logp over the mask = 1 rows of sequence s      -> ell[2P]
+ *   mask: 0 = not supervised, 2 = prompt row (ignored here: see ORPO_PREF_ORPO_FULL),
+ *         any other nonzero value = response row
+ *   l_s  = mean of logp over the response rows of sequence s     -> ell[2P]
  *   x_p  = (l_w - l_r) - (log1mexp(l_w) - log1mexp(l_r)), log1mexp(x) = log(1 - e^x)
  *   loss = (1/P) sum_p [ -l_w + lambda * softplus(-x_p) ]  (NLL over the chosen response)
  *   out[0..4] = loss, nll = mean(-l_w), or = mean(softplus(-x)),
@@ -141,12 +143,27 @@ int orpo_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int
  *   ORPO_PREF_DPO   : -log sigmoid(beta D)
  *   ORPO_PREF_IPO   : (D - 1/(2 beta))^2            (beta > 0)
  *   ORPO_PREF_HINGE : max(0, 1 - beta D)
+ *   ORPO_PREF_ORPO_FULL : ORPO with sft_scope = full (design page §1,
+ *                     combineFullNll): the NLL is the token mean of -logp over
+ *                     the chosen sequence's prompt rows (mask = 2) and response
+ *                     rows, -((P-1) pm + M l_w) / ((P-1) + M); the log-odds keep
+ *                     response-only means; beta = lambda
+ * Mask values for every kind: 0 = row not supervised; 2 = prompt row, read by the
+ * head like a response row but seen only by the full-scope NLL (it gets g = 0
+ * otherwise); any other nonzero value = response row.
  * loss = mean over pairs; out[0..4] = loss, mean(-statistic_w), mean preference
  * term, accuracy (chosen statistic beats rejected: l_w > l_r, or D > 0), margin
  * (mean of the argument of the term: x, beta((l_w-l_r)-gamma), beta D, D, beta D).
  * g[t] = d loss / d logp[t]: G_s / n_s for the mean kinds, G_s for the sum kinds.
  */
-enum { ORPO_PREF_ORPO = 0, ORPO_PREF_SIMPO = 1, ORPO_PREF_DPO = 2, ORPO_PREF_IPO = 3, ORPO_PREF_HINGE = 4 };
+enum {
+  ORPO_PREF_ORPO = 0,
+  ORPO_PREF_SIMPO = 1,
+  ORPO_PREF_DPO = 2,
+  ORPO_PREF_IPO = 3,
+  ORPO_PREF_HINGE = 4,
+  ORPO_PREF_ORPO_FULL = 5
+};
 int orpo_pref_loss(int kind, const float* logp, const int32_t* seq_id, const uint8_t* mask, int64_t M,
                    int32_t n_pairs, float beta, float gamma, const float* ref_logp, float* out, float* ell,
                    float* g, int32_t* status, void* stream);

@@ -166,7 +166,7 @@ def orpo_loss(logp, seq_id, mask, n_pairs, lam, out, ell, g, status, stream=None
                             _ptr(ell), _ptr(g), _ptr(status), _stream(stream)), "orpo_loss")
 
 
-PREF_KINDS = {"orpo": 0, "simpo": 1, "dpo": 2, "ipo": 3, "hinge": 4}
+PREF_KINDS = {"orpo": 0, "simpo": 1, "dpo": 2, "ipo": 3, "hinge": 4, "orpo_full": 5}
 
 
 def orpo_pref_loss(kind, logp, seq_id, mask, n_pairs, beta, gamma, ref_logp, out, ell, g, status, stream=None):

@@ -216,7 +216,7 @@ int orpo_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int
 int orpo_pref_loss(int kind, const float* logp, const int32_t* seq_id, const uint8_t* mask, int64_t M,
                    int32_t n_pairs, float beta, float gamma, const float* ref_logp, float* out, float* ell, float* g,
                    int32_t* status, void* stream) {
-  if (kind < ORPO_PREF_ORPO || kind > ORPO_PREF_HINGE) return ORPO_ERR_ARG;
+  if (kind < ORPO_PREF_ORPO || kind > ORPO_PREF_ORPO_FULL) return ORPO_ERR_ARG;
   if (M < 0 || M > kMaxRows || n_pairs < 1 || n_pairs > ORPO_MAX_PAIRS) return ORPO_ERR_SHAPE;
   const bool needs_ref = kind == ORPO_PREF_DPO || kind == ORPO_PREF_IPO || kind == ORPO_PREF_HINGE;
   if (!out || !ell || !status || (M > 0 && (!logp || !seq_id || !mask || !g)) || (needs_ref && !ref_logp))

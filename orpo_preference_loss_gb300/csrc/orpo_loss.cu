@@ -28,17 +28,20 @@ namespace orpo {
 namespace {
 
 constexpr int T = 1024;
-constexpr int kKindOrpo = 0, kKindSimpo = 1, kKindDpo = 2, kKindIpo = 3, kKindHinge = 4;
+constexpr int kKindOrpo = 0, kKindSimpo = 1, kKindDpo = 2, kKindIpo = 3, kKindHinge = 4, kKindOrpoFull = 5;
+constexpr uint8_t kPromptRow = 2;  // mask value: prompt row, supervised only by the full-scope NLL
 constexpr int32_t kSeqErr = 1 << 5, kEmptyErr = 1 << 6, kNonfiniteErr = 1 << 7;
 
 struct LossSmem {
   int head_sid[T], tail_sid[T], first_sid[T], last_sid[T];
-  int head_cnt[T], tail_cnt[T];
+  int head_cnt[T], tail_cnt[T];          // response rows of the partial runs
+  int head_fcnt[T], tail_fcnt[T];        // response + prompt rows (full-scope NLL)
   double head_sum[T], tail_sum[T];
+  double head_fsum[T], tail_fsum[T];
   double red[5][T / 32];
   int err;
 };
-// followed by: double seq_sum[S]; int seq_cnt[S]; double G[S]
+// followed by: double seq_sum[S]; int seq_cnt[S]; double G[S]; double seq_fsum[S]; int seq_fcnt[S]
 
 __device__ __forceinline__ double log1mexp_d(double x) {
   // log(1 - e^x), x <= 0; two branches at -ln 2 (Maechler 2012)
@@ -63,15 +66,21 @@ __global__ void __launch_bounds__(T, 1)
   double* seq_sum = reinterpret_cast<double*>(raw + sizeof(LossSmem));
   int* seq_cnt = reinterpret_cast<int*>(seq_sum + S);
   double* G = reinterpret_cast<double*>(raw + sizeof(LossSmem) + (size_t)S * 8 + (((size_t)S * 4 + 7) & ~size_t(7)));
+  double* seq_fsum = G + S;
+  int* seq_fcnt = reinterpret_cast<int*>(seq_fsum + S);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const double lam = (double)lam_f;  // lambda for ORPO, beta for the other kinds
   const double gam = (double)gamma_f;
-  const bool mean_kind = kind == kKindOrpo || kind == kKindSimpo;
+  const bool orpo_kind = kind == kKindOrpo || kind == kKindOrpoFull;
+  const bool mean_kind = orpo_kind || kind == kKindSimpo;
+  const bool full_scope = kind == kKindOrpoFull;
 
   if (tid == 0) sm.err = 0;
   for (int s = tid; s < S; s += T) {
     seq_sum[s] = 0.0;
     seq_cnt[s] = 0;
+    seq_fsum[s] = 0.0;
+    seq_fcnt[s] = 0;
   }
   __syncthreads();
 
@@ -80,10 +89,10 @@ __global__ void __launch_bounds__(T, 1)
   {
     const int chunk = (M + T - 1) / T;
     const int t0 = min(M, tid * chunk), t1 = min(M, t0 + chunk);
-    int cur = -1, cnt = 0, nruns = 0, last = -1, first = -1;
-    double sum = 0.0;
-    int hs = -1, hc = 0, ts = -1, tc = 0;
-    double hsum = 0.0, tsum = 0.0;
+    int cur = -1, cnt = 0, fcnt = 0, nruns = 0, last = -1, first = -1;
+    double sum = 0.0, fsum = 0.0;
+    int hs = -1, hc = 0, hfc = 0, ts = -1, tc = 0, tfc = 0;
+    double hsum = 0.0, hfsum = 0.0, tsum = 0.0, tfsum = 0.0;
     for (int t = t0; t < t1; ++t) {
       const int sid = seq_id[t];
       if (sid == -1) continue;
@@ -95,38 +104,49 @@ __global__ void __launch_bounds__(T, 1)
       if (sid != cur) {
         if (cur >= 0) {
           if (nruns == 0) {
-            hs = cur, hsum = sum, hc = cnt;
+            hs = cur, hsum = sum, hc = cnt, hfsum = fsum, hfc = fcnt;
           } else {
             seq_sum[cur] = sum;  // a run strictly inside the chunk is the whole sequence
             seq_cnt[cur] = cnt;
+            seq_fsum[cur] = fsum;
+            seq_fcnt[cur] = fcnt;
           }
           ++nruns;
         }
         cur = sid;
-        sum = 0.0;
-        cnt = 0;
+        sum = fsum = 0.0;
+        cnt = fcnt = 0;
       }
-      if (mask[t] != 0) {
-        sum += (double)logp[t];
-        ++cnt;
+      const uint8_t mk = mask[t];
+      if (mk != 0) {
+        const double v = (double)logp[t];
+        fsum += v;
+        ++fcnt;
+        if (mk != kPromptRow) {
+          sum += v;
+          ++cnt;
+        }
       }
       last = sid;
       if (first < 0) first = sid;
     }
     if (cur >= 0) {
       if (nruns == 0) {
-        hs = cur, hsum = sum, hc = cnt;
+        hs = cur, hsum = sum, hc = cnt, hfsum = fsum, hfc = fcnt;
       } else {
-        ts = cur, tsum = sum, tc = cnt;
-        // the previously flushed run was written as interior; if it was the head it is in hs
+        ts = cur, tsum = sum, tc = cnt, tfsum = fsum, tfc = fcnt;
       }
     }
     sm.head_sid[tid] = hs;
     sm.head_sum[tid] = hsum;
     sm.head_cnt[tid] = hc;
+    sm.head_fsum[tid] = hfsum;
+    sm.head_fcnt[tid] = hfc;
     sm.tail_sid[tid] = ts;
     sm.tail_sum[tid] = tsum;
     sm.tail_cnt[tid] = tc;
+    sm.tail_fsum[tid] = tfsum;
+    sm.tail_fcnt[tid] = tfc;
     sm.first_sid[tid] = first;
     sm.last_sid[tid] = last;
   }
@@ -144,26 +164,34 @@ __global__ void __launch_bounds__(T, 1)
 
   // ---- phase 2: add the partial head / tail runs of every chunk to their sequence
   for (int s = warp; s < S; s += T / 32) {
-    double acc = 0.0;
-    int c = 0;
+    double acc = 0.0, facc = 0.0;
+    int c = 0, fc = 0;
     for (int i = lane; i < T; i += 32) {
       if (sm.head_sid[i] == s) {
         acc += sm.head_sum[i];
         c += sm.head_cnt[i];
+        facc += sm.head_fsum[i];
+        fc += sm.head_fcnt[i];
       }
       if (sm.tail_sid[i] == s) {
         acc += sm.tail_sum[i];
         c += sm.tail_cnt[i];
+        facc += sm.tail_fsum[i];
+        fc += sm.tail_fcnt[i];
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       acc += __shfl_xor_sync(0xffffffffu, acc, o);
       c += __shfl_xor_sync(0xffffffffu, c, o);
+      facc += __shfl_xor_sync(0xffffffffu, facc, o);
+      fc += __shfl_xor_sync(0xffffffffu, fc, o);
     }
     if (lane == 0) {
       seq_sum[s] += acc;
       seq_cnt[s] += c;
+      seq_fsum[s] += facc;
+      seq_fcnt[s] += fc;
     }
   }
   __syncthreads();
@@ -185,17 +213,20 @@ __global__ void __launch_bounds__(T, 1)
   double c_loss = 0.0, c_nll = 0.0, c_or = 0.0, c_acc = 0.0, c_mar = 0.0;
   for (int p = tid; p < P; p += T) {
     const double lw = seq_sum[2 * p], lr = seq_sum[2 * p + 1];
-    double term = 0.0, dw = 0.0, margin = 0.0, Gw, Gr, loss_p;
+    double term = 0.0, dw = 0.0, margin = 0.0, Gw, Gr, loss_p, nll_p = -lw;
     bool better;
-    if (kind == kKindOrpo) {
-      // x = (l_w - l_r) - (log1mexp(l_w) - log1mexp(l_r)); loss_p = -l_w + lambda softplus(-x)
+    if (orpo_kind) {
+      // x = (l_w - l_r) - (log1mexp(l_w) - log1mexp(l_r)); loss_p = NLL_p + lambda softplus(-x)
       const double x = (lw - lr) - (log1mexp_d(lw) - log1mexp_d(lr));
       term = softplus_d(-x);
       const double sg = sigmoid_d(-x);
       const double inv_w = -1.0 / expm1(lw), inv_r = -1.0 / expm1(lr);  // 1 / (1 - e^l)
-      Gw = (-1.0 - lam * sg * inv_w) / (double)P;
+      // response scope folds the NLL gradient (-1/P on l_w) into G_w; full scope spreads
+      // -1/(P N_w) over the chosen prompt + response rows in phase 5
+      if (full_scope) nll_p = -seq_fsum[2 * p] / (double)seq_fcnt[2 * p];
+      Gw = ((full_scope ? 0.0 : -1.0) - lam * sg * inv_w) / (double)P;
       Gr = (lam * sg * inv_r) / (double)P;
-      loss_p = -lw + lam * term;
+      loss_p = nll_p + lam * term;
       margin = x;
       better = lw > lr;
       if (lw > 0.0 || lr > 0.0) err |= kNonfiniteErr;
@@ -233,7 +264,7 @@ __global__ void __launch_bounds__(T, 1)
     G[2 * p] = Gw;
     G[2 * p + 1] = Gr;
     c_loss += loss_p;
-    c_nll += -lw;
+    c_nll += nll_p;
     c_or += term;
     c_acc += better ? 1.0 : 0.0;
     c_mar += margin;
@@ -262,12 +293,14 @@ __global__ void __launch_bounds__(T, 1)
   // ---- phase 5: per-token gradient
   for (int t = tid; t < M; t += T) {
     const int sid = seq_id[t];
-    float gv = 0.f;
-    if (sid >= 0 && sid < S && mask[t] != 0) {
+    const uint8_t mk = mask[t];
+    double gv = 0.0;
+    if (sid >= 0 && sid < S && mk != 0) {
       const int n = seq_cnt[sid];
-      if (n > 0) gv = (float)(mean_kind ? G[sid] / (double)n : G[sid]);
+      if (mk != kPromptRow && n > 0) gv = mean_kind ? G[sid] / (double)n : G[sid];
+      if (full_scope && (sid & 1) == 0 && seq_fcnt[sid] > 0) gv += -1.0 / ((double)P * seq_fcnt[sid]);
     }
-    g[t] = gv;
+    g[t] = (float)gv;
   }
 }
 
@@ -275,7 +308,7 @@ __global__ void __launch_bounds__(T, 1)
 
 size_t loss_smem_bytes(int P) {
   const size_t S = 2 * (size_t)P;
-  return sizeof(LossSmem) + S * 8 + ((S * 4 + 7) & ~size_t(7)) + S * 8;
+  return sizeof(LossSmem) + S * 8 + ((S * 4 + 7) & ~size_t(7)) + S * 8 + S * 8 + S * 4;
 }
 
 cudaError_t launch_loss(int kind, const float* logp, const int32_t* seq_id, const uint8_t* mask, int M, int P,

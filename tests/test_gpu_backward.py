@@ -96,3 +96,30 @@ def test_zero_rows_give_zero_gradient():
     t = to_dev(w)
     dh, dW, st = gpu_backward(t, lse, g, w.M, w.V, w.d, w.softcap)
     assert st == 0 and np.all(dh == 0) and np.all(dW == 0)
+
+
+def test_full_scope_chain():
+    """sft_scope = full: prompt rows (mask 2) go through the head and the NLL."""
+    w = workloads.make("tiny")
+    mask = w.mask.copy()
+    mask[mask == 0] = 2          # the recipe's 8 prompt rows per sequence become supervised prompt rows
+    w.mask = mask
+    logp_r, lse_r, res, dh_r, dW_r = oracle.full_chain(f64(w.h), f64(w.W), w.targets, mask, w.seq_id, w.n_pairs,
+                                                       w.lam, w.softcap, scope="full")
+    t = to_dev(w)
+    logp, lse, st = gpu_forward(t, w.M, w.V, w.d, w.softcap)
+    assert st == 0 and np.max(np.abs(logp - logp_r)) < LOGP_ATOL
+    import orpo_preference_loss_gb300 as orpo
+    out = torch.empty(5, device=dev())
+    ell = torch.empty(2 * w.n_pairs, device=dev())
+    g = torch.empty(w.M, device=dev())
+    stt = torch.zeros(1, dtype=torch.int32, device=dev())
+    orpo.orpo_pref_loss("orpo_full", torch.from_numpy(logp).to(dev()), t["seq_id"], t["mask"], w.n_pairs, w.lam,
+                        0.0, None, out, ell, g, stt)
+    torch.cuda.synchronize()
+    assert int(stt.item()) == 0
+    assert abs(float(out[0]) - res.loss) <= LOSS_RTOL * abs(res.loss)
+    dh, dW, st = gpu_backward(t, lse, g.cpu().numpy(), w.M, w.V, w.d, w.softcap)
+    assert st == 0
+    assert relfro(dh, dh_r) < GRAD_RELFRO and relfro(dW, dW_r) < GRAD_RELFRO
+    assert np.abs(dh[mask == 2]).sum() > 0      # prompt rows of chosen sequences carry gradient now

@@ -55,3 +55,28 @@ def test_dpo_policy_equal_reference_gives_log2_on_gpu():
     ref = np.bincount(seq, weights=logp.astype(np.float64)).astype(np.float32)
     out, _, g, st = run("dpo", logp, seq, mask, 4, 0.3, 0.0, ref)
     assert st == 0 and abs(out[0] - np.log(2.0)) < 1e-6 and abs(out[4]) < 1e-5
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "ragged"])
+def test_orpo_full_scope_matches_oracle(name):
+    w = workloads.make(name, d=8, V=16)
+    mask = w.mask.copy()
+    rng = np.random.default_rng(8)
+    # turn the first rows of every sequence into supervised prompt rows (mask 2)
+    for s in range(2 * w.n_pairs):
+        rows = np.where(w.seq_id == s)[0]
+        k = int(rng.integers(0, max(1, len(rows) // 3)))
+        mask[rows[:k]] = 2
+        mask[rows[-1]] = 1
+    logp = workloads.synthetic_logp(6, w.seq_id, mask, scale=0.5, offset=-1.0)
+    out, ell, g, st = run("orpo_full", logp, w.seq_id, mask, w.n_pairs, 0.1, 0.0, None)
+    assert st == 0
+    r = oracle.orpo_loss(logp.astype(np.float64), w.seq_id, mask, w.n_pairs, 0.1, scope="full")
+    for a, b in zip(out, r.metrics()):
+        assert abs(a - b) <= LOSS_RTOL * max(abs(b), 1e-6), (out, r.metrics())
+    assert np.allclose(ell, r.ell, rtol=1e-6, atol=1e-6)
+    assert np.allclose(g, r.g, rtol=1e-5, atol=1e-12)
+    # response scope on the same mask: prompt rows carry no gradient
+    out2, _, g2, st2 = run("orpo", logp, w.seq_id, mask, w.n_pairs, 0.1, 0.0, None)
+    r2 = oracle.orpo_loss(logp.astype(np.float64), w.seq_id, mask, w.n_pairs, 0.1)
+    assert st2 == 0 and np.allclose(g2, r2.g, rtol=1e-5, atol=1e-12) and np.all(g2[mask == 2] == 0)
