@@ -49,37 +49,67 @@ struct RecArgs {
 
 // dZ for 32 accumulator values of one row starting at vocabulary column col0;
 // writes 16 packed bf16 pairs into w[0..15].
-//   softcap on : z~ = c (1 - 2q), q = 1 / (1 + e^{2z/c}),  sech^2(z/c) = 4 q (1 - q)
+//   softcap on : t = tanh(z / c) = 1 - 2q, q = 1 / (1 + e^{2z/c}), z~ = c t,
+//                sech^2(z/c) = 4q(1 - q); for caps above kCapExpMax, |z / c| < 1/8 uses the
+//                Taylor form of t and 1 - t^2 (the forward's hybrid form)
 //   dZ = g sech^2 (onehot - 2^(x - lse2)),  x = z~ log2(e)
+constexpr int kCapOff = 0, kCapExp = 1, kCapHybrid = 2;  // softcap forms, as in the forward
+constexpr float kCapExpMax = 64.f;
+
+template <int cap>
 __device__ __forceinline__ void dz_chunk(const uint32_t (&r)[32], int col0, int V, int y, float gval, float lse2,
-                                         bool cap, float K, float A, float B2, uint32_t* w) {
-  float dz[32];
+                                         float inv_c, float cl2, uint32_t* w) {
+  float dz[32], sl[32];
+  if constexpr (cap == kCapExp) {
+    const float K = 2.f * kLog2e * inv_c, A = cl2 - lse2, B2 = 2.f * cl2;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float z = __uint_as_float(r[i]);
-    float x, gs;
-    if (cap) {
-      const float q = rcp_approx(1.f + ex2_approx(z * K));
-      x = fmaf(-B2, q, A);
-      gs = gval * (4.f * q * (1.f - q));
-    } else {
-      x = z * kLog2e;
-      gs = gval;
+    for (int i = 0; i < 32; ++i) {
+      const float q = rcp_approx(1.f + ex2_approx(__uint_as_float(r[i]) * K));
+      sl[i] = 4.f * q * (1.f - q);
+      dz[i] = -(gval * sl[i]) * ex2_approx(fmaf(-B2, q, A));  // 2^(x - lse2), x = A' - 2A' q
     }
-    dz[i] = -gs * ex2_approx(x - lse2);
+  } else if constexpr (cap == kCapHybrid) {
+    bool big = false;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      dz[i] = __uint_as_float(r[i]) * inv_c;  // u = z / c
+      big |= fabsf(dz[i]) >= kTanhSmall;
+    }
+    if (__any_sync(0xffffffffu, big)) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float u = dz[i];
+        float q = 0.5f, t;
+        if (fabsf(u) < kTanhSmall) {
+          t = tanh_small(u);
+          sl[i] = fmaf(-t, t, 1.f);
+        } else {
+          t = tanh_exp(u, &q);
+          sl[i] = 4.f * q * (1.f - q);
+        }
+        dz[i] = t * cl2;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float t = tanh_small(dz[i]);
+        sl[i] = fmaf(-t, t, 1.f);
+        dz[i] = t * cl2;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) dz[i] = -(gval * sl[i]) * ex2_approx(dz[i] - lse2);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      sl[i] = 1.f;
+      dz[i] = -gval * ex2_approx(__uint_as_float(r[i]) * kLog2e - lse2);
+    }
   }
   if ((unsigned)(y - col0) < 32u) {  // the target column lies in this chunk: add g * sech^2 there
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (i == y - col0) {
-        float gs = gval;
-        if (cap) {
-          const float q = rcp_approx(1.f + ex2_approx(__uint_as_float(r[i]) * K));
-          gs = gval * (4.f * q * (1.f - q));
-        }
-        dz[i] += gs;
-      }
-    }
+    for (int i = 0; i < 32; ++i)
+      if (i == y - col0) dz[i] += gval * sl[i];
   }
   if (col0 + 32 > V) {
 #pragma unroll
@@ -90,6 +120,7 @@ __device__ __forceinline__ void dz_chunk(const uint32_t (&r)[32], int col0, int 
   for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(dz[2 * i], dz[2 * i + 1]);
 }
 
+template <int cap>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     rec_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mw,
                const __grid_constant__ CUtensorMap ms, RecSched sched, RecArgs p) {
@@ -104,10 +135,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   run_cta(sched, feed, p.status, [&](uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
     const int q = warp & 3;
     const uint32_t staging = smem_u32(smem + SMEM_STAGING_OFF + (warp - 2) * STAGING_PER_WARP);
-    const bool cap = p.softcap > 0.f;
-    const float K = cap ? 2.f * kLog2e / p.softcap : 0.f;
-    const float A = cap ? p.softcap * kLog2e : 0.f;
-    const float B2 = 2.f * A;
+    const float inv_c = cap != kCapOff ? 1.f / p.softcap : 0.f;
+    const float cl2 = p.softcap * kLog2e;
     uint32_t tcount = 0, nstore = 0;
     for (uint32_t i = 0;; ++i, ++tcount) {
       const int u = feed_consume(feed, ctl, i, p.status, true);
@@ -141,10 +170,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else {
           tmem_ld_wait(ra);
           tmem_ld32(taddr + gi * 64 + 32, rb);
-          dz_chunk(ra, vcol0 + gi * 64, p.V, y, gval, lse2, cap, K, A, B2, w);
+          dz_chunk<cap>(ra, vcol0 + gi * 64, p.V, y, gval, lse2, inv_c, cl2, w);
           tmem_ld_wait(rb);
           if (gi + 1 < BN / 64) tmem_ld32(taddr + gi * 64 + 64, ra);
-          dz_chunk(rb, vcol0 + gi * 64 + 32, p.V, y, gval, lse2, cap, K, A, B2, w + 16);
+          dz_chunk<cap>(rb, vcol0 + gi * 64 + 32, p.V, y, gval, lse2, inv_c, cl2, w + 16);
         }
         const uint32_t box = staging + (nstore & 1u) * BOX_BYTES;
         if (lane == 0) bulk_wait_group_read<1>();  // the store that used this buffer has read it
@@ -294,21 +323,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st) {
+namespace {
+template <int cap>
+cudaError_t launch_rec_kernel(const RecLaunch& L, cudaStream_t st) {
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(rec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+    cudaError_t e = cudaFuncSetAttribute(rec_kernel<cap>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
   RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks};
   RecArgs a{L.targets, L.mask, L.lse, L.g, L.M, L.V, L.softcap, L.status};
   prof_begin(K_REC, st);
-  rec_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, L.ms_store, sched, a);
+  rec_kernel<cap><<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, L.ms_store, sched, a);
   prof_end(K_REC, st);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st) {
+  const int cap = L.softcap > 0.f ? (L.softcap <= kCapExpMax ? kCapExp : kCapHybrid) : kCapOff;
+  return cap == kCapExp      ? launch_rec_kernel<kCapExp>(L, st)
+         : cap == kCapHybrid ? launch_rec_kernel<kCapHybrid>(L, st)
+                             : launch_rec_kernel<kCapOff>(L, st);
 }
 
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {

@@ -58,16 +58,48 @@ struct RowState {
   float m, s;
 };
 
+// Softcap forms (chosen once per launch):
+//   kCapExp    (c <= kCapExpMax): tanh u = 1 - 2 / (1 + e^{2u}); one ex2 + one rcp per logit,
+//              absolute error ~ c * 2^-22 on z~ (<= 1.5e-5 at c = 64).
+//   kCapHybrid (larger c): the same form loses ~c * 2^-23 to cancellation, so |u| < 1/8 uses the
+//              Taylor series of tanh (tanh_small) and only larger |u| the exp form; the exp form
+//              runs only when some lane of the warp needs it.
+constexpr int kCapOff = 0, kCapExp = 1, kCapHybrid = 2;
+constexpr float kCapExpMax = 64.f;
+
 // Fold 32 logits (raw fp32 accumulator bits) starting at column col0 into the row state.
-__device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, int V, int y, bool cap, float K,
-                                           float A, float B2, RowState& st, float* tgt_slot) {
+// x = z~ log2(e) (base-2 units), z~ = c tanh(z / c) with the softcap on, else z.
+template <int cap>
+__device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, int V, int y, float inv_c, float cl2,
+                                           RowState& st, float* tgt_slot) {
   if (col0 >= V) return;
   float x[32];
+  if constexpr (cap == kCapExp) {
+    // x = c log2e (1 - 2 / (1 + 2^{z K})) = A - 2A / (1 + 2^{z K}),  A = c log2e, K = 2 log2e / c
+    const float K = 2.f * kLog2e * inv_c, A = cl2, B2 = 2.f * cl2;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float z = __uint_as_float(r[i]);
-    // softcap: z~ = c tanh(z/c) = c (1 - 2 / (1 + e^{2z/c})); in base-2 units x = A - B2 / (1 + 2^{zK})
-    x[i] = cap ? fmaf(-B2, rcp_approx(1.f + ex2_approx(z * K)), A) : z * kLog2e;
+    for (int i = 0; i < 32; ++i) x[i] = fmaf(-B2, rcp_approx(1.f + ex2_approx(__uint_as_float(r[i]) * K)), A);
+  } else if constexpr (cap == kCapHybrid) {
+    bool big = false;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      x[i] = __uint_as_float(r[i]) * inv_c;  // u = z / c
+      big |= fabsf(x[i]) >= kTanhSmall;
+    }
+    if (__any_sync(0xffffffffu, big)) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float q;
+        const float u = x[i];
+        x[i] = (fabsf(u) < kTanhSmall ? tanh_small(u) : tanh_exp(u, &q)) * cl2;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = tanh_small(x[i]) * cl2;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]) * kLog2e;
   }
   if (col0 + 32 > V) {
 #pragma unroll
@@ -102,6 +134,7 @@ __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, in
   st.m = mnew;
 }
 
+template <int cap>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mw, FwdSched sched,
                FwdArgs p) {
@@ -114,10 +147,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const Feed feed{nullptr, sched.num_units()};
   run_cta(sched, feed, p.status, [&](uint8_t*, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
     const int q = warp & 3;
-    const bool cap = p.softcap > 0.f;
-    const float K = cap ? 2.f * kLog2e / p.softcap : 0.f;
-    const float A = cap ? p.softcap * kLog2e : 0.f;
-    const float B2 = 2.f * A;
+    const float inv_c = cap != kCapOff ? 1.f / p.softcap : 0.f;
+    const float cl2 = p.softcap * kLog2e;
     uint32_t tcount = 0;
     for (uint32_t i = 0;; ++i) {
       const int u = feed_consume(feed, ctl, i, p.status, true);
@@ -140,10 +171,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int c = 0; c < BN / 32; c += 2) {
           tmem_ld_wait(ra);
           tmem_ld32(taddr + (c + 1) * 32, rb);
-          fold_chunk(ra, col_base + c * 32, p.V, y, cap, K, A, B2, st, tgt_slot);
+          fold_chunk<cap>(ra, col_base + c * 32, p.V, y, inv_c, cl2, st, tgt_slot);
           tmem_ld_wait(rb);
           if (c + 2 < BN / 32) tmem_ld32(taddr + (c + 2) * 32, ra);
-          fold_chunk(rb, col_base + (c + 1) * 32, p.V, y, cap, K, A, B2, st, tgt_slot);
+          fold_chunk<cap>(rb, col_base + (c + 1) * 32, p.V, y, inv_c, cl2, st, tgt_slot);
         }
         epi_release(ctl, tcount);
       }
@@ -180,23 +211,31 @@ __global__ void merge_kernel(const float* __restrict__ part_m, const float* __re
   if (err) atomicOr(status, err);
 }
 
-}  // namespace
-
-cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st) {
+template <int cap>
+cudaError_t launch_fwd_kernel(const FwdLaunch& L, cudaStream_t st) {
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<cap>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
   FwdSched sched{nullptr, nullptr, L.n_mt, L.nsplit, L.n_vt, L.kblocks};
   FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M, L.Mpad, L.V, L.softcap, L.status};
   prof_begin(K_FWD, st);
-  fwd_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, sched, a);
+  fwd_kernel<cap><<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, sched, a);
   prof_end(K_FWD, st);
-  cudaError_t e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st) {
+  const int cap = L.softcap > 0.f ? (L.softcap <= kCapExpMax ? kCapExp : kCapHybrid) : kCapOff;
+  cudaError_t e = cap == kCapExp      ? launch_fwd_kernel<kCapExp>(L, st)
+                  : cap == kCapHybrid ? launch_fwd_kernel<kCapHybrid>(L, st)
+                                      : launch_fwd_kernel<kCapOff>(L, st);
   if (e != cudaSuccess) return e;
   const int threads = 256;
   prof_begin(K_MERGE, st);

@@ -201,6 +201,24 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
+// tanh(u) for |u| < 1/8 from its Taylor series u - u^3/3 + 2u^5/15 - 17u^7/315 (next term
+// 62u^9/2835 < 2e-10 relative there): no cancellation, so c * tanh(z / c) keeps full relative
+// precision however large the cap c is.
+__device__ __forceinline__ float tanh_small(float u) {
+  const float u2 = u * u;
+  return u * fmaf(u2, fmaf(u2, fmaf(u2, -17.f / 315.f, 2.f / 15.f), -1.f / 3.f), 1.f);
+}
+
+// tanh(u) = 1 - 2q with q = 1 / (1 + 2^{2u log2 e}); exact to ~1 ulp of 1 for any u (saturates to +-1);
+// returns q too, since 1 - tanh^2 = 4q(1 - q) without cancellation.
+__device__ __forceinline__ float tanh_exp(float u, float* q_out) {
+  const float q = rcp_approx(1.f + ex2_approx(u * 2.8853900817779268f));  // 2 log2(e)
+  *q_out = q;
+  return fmaf(-2.f, q, 1.f);
+}
+
+constexpr float kTanhSmall = 0.125f;
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
