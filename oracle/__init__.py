@@ -17,5 +17,6 @@ from .orpo_oracle import (  # noqa: F401
     full_chain,
     pref_loss,
     PREF_KINDS,
+    dequant_affine,
     OracleError,
 )

@@ -25,6 +25,9 @@ segmented backward)" page, and the "Steel flash-CCE — handoff" page):
   — design" §8.3 SimPO; the xtrain post-training page, Stage P1, for DPO's
   summed sequence log-prob with cached reference log-probs; IPO and hinge are
   named there without formulas and take their standard forms).
+* ``dequant_affine`` — the quantised head's weights (§5.1 tier 4: the head is
+  4/8-bit affine group-quantised with scales and biases; here dequantised to
+  bf16 before the contraction, see the function).
 * ``head_backward`` — implementation spec, backward bullet: recompute the
   logits, ``dZ = g * (onehot_y - softmax(z~)) * sech^2(z / c)``, then
   ``dh = dZ W`` and (the head-weight gradient that the pages leave to the
@@ -392,3 +395,43 @@ def pref_loss(kind: str, logp, seq_id, mask, n_pairs: int, beta: float, gamma: f
         raise OracleError("nonfinite", "loss is not finite")
     return LossResult(loss=loss, nll=float(np.mean(-w)), orr=loss, accuracy=float(np.mean(chosen_better)),
                       margin=float(np.mean(margin)), ell=ell, log_odds=margin, g=g, n=n)
+
+
+# --------------------------------------------------------------------------
+# quantized head: affine group dequantisation
+# --------------------------------------------------------------------------
+
+def _round_bf16(x32: np.ndarray) -> np.ndarray:
+    """fp32 -> nearest-even bf16, returned as float64 values."""
+    u = np.ascontiguousarray(x32, dtype=np.float32).view(np.uint32)
+    r = (u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))) >> np.uint32(16)
+    return (r.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def dequant_affine(wq: np.ndarray, scales_bits: np.ndarray, biases_bits: np.ndarray, bits: int, group: int,
+                   d: int) -> np.ndarray:
+    """Weights of an affine group-quantised head ("Training — design" §5.1 tier 4: 4/8-bit affine
+    dequant with per-group scales and biases).
+
+    wq: uint8 [V, d * bits / 8]; for 4 bits element j of a row is the low nibble of byte j/2 when j
+    is even and the high nibble when j is odd; for 8 bits it is byte j.  scales, biases: bf16 bit
+    patterns [V, d / group].  The head's weight is W[v, j] = bf16(scale * q + bias), the product and
+    sum taken in fp32 (the product of a bf16 scale and q < 256 is exact) and rounded once to bf16,
+    nearest even.  Returns W as float64 [V, d].
+    """
+    wq = np.asarray(wq, dtype=np.uint8)
+    V = wq.shape[0]
+    if bits == 4:
+        q = np.empty((V, d), dtype=np.uint8)
+        q[:, 0::2] = wq & 0x0F
+        q[:, 1::2] = wq >> 4
+    elif bits == 8:
+        q = wq[:, :d]
+    else:
+        raise OracleError("arg", "bits must be 4 or 8")
+    s = bf16_bits_to_f64(scales_bits).astype(np.float32)
+    b = bf16_bits_to_f64(biases_bits).astype(np.float32)
+    s_full = np.repeat(s, group, axis=1)[:, :d]
+    b_full = np.repeat(b, group, axis=1)[:, :d]
+    w32 = s_full * q.astype(np.float32) + b_full
+    return _round_bf16(w32)

@@ -226,3 +226,29 @@ def synthetic_logp(seed: int, seq_id: np.ndarray, mask: np.ndarray, scale: float
     r = _rng(seed, 9)
     x = offset - scale * np.abs(r.standard_normal(len(seq_id)))
     return np.minimum(x, -1e-3).astype(np.float32)
+
+
+def quantize_affine(W_bits: np.ndarray, bits: int, group: int):
+    """Affine group quantisation of bf16 weights (input preparation for the quantised head).
+
+    Per row and group of `group` consecutive columns: bias = min, scale = (max - min) / (2^bits - 1),
+    both rounded to bf16; q = clip(round((w - bias) / scale), 0, 2^bits - 1).  Returns
+    (wq uint8 [V, d * bits / 8], scales bf16 bits [V, d / group], biases bf16 bits [V, d / group]);
+    4-bit values are packed two per byte, even column in the low nibble.
+    """
+    W = bf16_to_f32(W_bits).astype(np.float64)
+    V, d = W.shape
+    g = W.reshape(V, d // group, group)
+    lo, hi = g.min(axis=2), g.max(axis=2)
+    levels = (1 << bits) - 1
+    scale = np.where(hi > lo, (hi - lo) / levels, 1.0)
+    s_bits = round_bf16(scale.astype(np.float32))
+    b_bits = round_bf16(lo.astype(np.float32))
+    s = bf16_to_f32(s_bits).astype(np.float64)[:, :, None]
+    b = bf16_to_f32(b_bits).astype(np.float64)[:, :, None]
+    q = np.clip(np.rint((g - b) / s), 0, levels).astype(np.uint8).reshape(V, d)
+    if bits == 4:
+        wq = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+    else:
+        wq = q
+    return np.ascontiguousarray(wq), s_bits, b_bits
