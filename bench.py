@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--loss", default="orpo", choices=["orpo", "simpo", "dpo", "ipo", "hinge", "orpo_full"],
                     help="preference objective between forward and backward (orpo_loss for orpo)")
+    ap.add_argument("--quant", type=int, default=0, choices=[0, 4, 8],
+                    help="run the quantised head: W as 4/8-bit affine groups of 64 (0 = bf16 head)")
+    ap.add_argument("--frozen", action="store_true", help="frozen head: skip dW")
     ap.add_argument("--M", type=int, default=None, help="shrink the workload's rows (profiling cases)")
     ap.add_argument("--V", type=int, default=None, help="shrink the vocabulary (profiling cases)")
     ap.add_argument("--d", type=int, default=None, help="change the hidden size (profiling cases)")
@@ -244,16 +247,23 @@ def ours(args, w, rank, world, local):
         "mask": torch.from_numpy(np.ascontiguousarray(w.mask)).pin_memory(),
         "seq_id": torch.from_numpy(np.ascontiguousarray(w.seq_id)).pin_memory(),
     }
+    if args.quant:
+        import workloads
+        wq, qs, qb = workloads.quantize_affine(w.W, args.quant, 64)
+        del host["W"]
+        host["wq"] = torch.from_numpy(wq).pin_memory()
+        host["qs"] = torch.from_numpy(qs.view(np.int16)).pin_memory()
+        host["qb"] = torch.from_numpy(qb.view(np.int16)).pin_memory()
     t = {k: v.to(dev) for k, v in host.items()}
     h_bf = t["h"].view(torch.bfloat16)
-    W_bf = t["W"].view(torch.bfloat16)
+    W_bf = None if args.quant else t["W"].view(torch.bfloat16)
     logp = torch.empty(M, dtype=torch.float32, device=dev)
     lse = torch.empty(M, dtype=torch.float32, device=dev)
     out = torch.empty(5, dtype=torch.float32, device=dev)
     ell = torch.empty(2 * P, dtype=torch.float32, device=dev)
     g = torch.empty(M, dtype=torch.float32, device=dev)
     dh = torch.empty((M, d), dtype=torch.float32, device=dev)
-    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    dW = None if args.frozen else torch.empty((V, d), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     # cached reference sums for the DPO-family objectives: seeded synthetic values per sequence
     ref = torch.from_numpy((-6.0 * np.bincount(np.maximum(w.seq_id, 0), minlength=2 * P)[:2 * P]
@@ -262,15 +272,24 @@ def ours(args, w, rank, world, local):
     torch.cuda.synchronize()
     mem_before = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)
-    ws = torch.empty(orpo.orpo_head_workspace_bytes(M, V, d), dtype=torch.uint8, device=dev)
+    ws_bytes = orpo.orpo_head_q_workspace_bytes(M, V, d) if args.quant else orpo.orpo_head_workspace_bytes(M, V, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if args.quant:
+        qw = (t["wq"], t["qs"].view(torch.bfloat16), t["qb"].view(torch.bfloat16), args.quant, 64)
 
     def step():
-        orpo.orpo_head_fwd(h_bf, W_bf, t["targets"], t["mask"], w.softcap, logp, lse, ws, status)
+        if args.quant:
+            orpo.orpo_head_fwd_q(h_bf, *qw, t["targets"], t["mask"], w.softcap, logp, lse, ws, status)
+        else:
+            orpo.orpo_head_fwd(h_bf, W_bf, t["targets"], t["mask"], w.softcap, logp, lse, ws, status)
         if args.loss == "orpo":
             orpo.orpo_loss(logp, t["seq_id"], t["mask"], P, w.lam, out, ell, g, status)
         else:
             orpo.orpo_pref_loss(args.loss, logp, t["seq_id"], t["mask"], P, beta, 0.5, ref, out, ell, g, status)
-        orpo.orpo_head_bwd(h_bf, W_bf, t["targets"], t["mask"], lse, g, w.softcap, dh, dW, False, ws, status)
+        if args.quant:
+            orpo.orpo_head_bwd_q(h_bf, *qw, t["targets"], t["mask"], lse, g, w.softcap, dh, dW, False, ws, status)
+        else:
+            orpo.orpo_head_bwd(h_bf, W_bf, t["targets"], t["mask"], lse, g, w.softcap, dh, dW, False, ws, status)
 
     for _ in range(args.warmup):
         step()
@@ -339,12 +358,12 @@ def ours(args, w, rank, world, local):
         return
 
     burst, sustained, hbm, src = peaks()
-    flops_step = 6.0 * M * V * d
+    flops_step = (4.0 if args.frozen else 6.0) * M * V * d
     tflops = world * flops_step * args.steps / (ms / 1e3) / 1e12
     # per-kernel algorithmic flops over the timed region (dense contractions each kernel computes)
     kflops = {"fwd_logits": 2.0 * M * V * d * args.steps,
               "bwd_recompute": 2.0 * M * V * d * args.steps,
-              "bwd_grad_gemm": 4.0 * M * V * d * args.steps}
+              "bwd_grad_gemm": (2.0 if args.frozen else 4.0) * M * V * d * args.steps}
     kernels = {}
     for name, (kms, cnt) in prof.items():
         if cnt == 0:
@@ -364,6 +383,8 @@ def ours(args, w, rank, world, local):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(workload_config(w), objective=args.loss,
+                           head=f"{args.quant}-bit affine groups of 64" if args.quant else "bf16",
+                           dW="skipped (frozen head)" if args.frozen else "computed",
                            parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
             "tflops": tflops, "frac_of_peak": tflops / sustained, "frac_of_burst_peak": tflops / burst,
             "peak_extra_gb": peak_extra / 1e9, "e2e": e2e, "gpu_launches": sum(v["launches"] for v in

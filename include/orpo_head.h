@@ -175,7 +175,9 @@ int orpo_pref_loss(int kind, const float* logp, const int32_t* seq_id, const uin
  *   dZ[t, v] = g[t] * (onehot(v == targets[t]) - p[t, v]) * sech^2(z[t, v] / softcap)
  *              (sech^2 factor only when softcap > 0; dZ = 0 on mask = 0 rows),
  *   dh  = dZ W     (fp32 [M, d], overwritten),
- *   dW  = dZ^T h   (fp32 [V, d]; overwritten, or added to when accumulate_dW != 0).
+ *   dW  = dZ^T h   (fp32 [V, d]; overwritten, or added to when accumulate_dW != 0;
+ *                  dW = NULL skips it: a frozen head needs dh only, and the
+ *                  backward then does two thirds of the work).
  * g is dloss/dlogp (what orpo_loss returns).  dZ is rounded to bf16 once, in a
  * bounded workspace block, before the two contractions; accumulation is fp32
  * and the result does not depend on run-to-run scheduling (no float atomics).
@@ -186,6 +188,36 @@ int orpo_head_bwd(const void* h_bf16, const void* W_bf16, const int32_t* targets
                   int64_t V, int64_t d, float softcap, float* dh, float* dW,
                   int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* status,
                   void* stream);
+
+/*
+ * Quantised head (design page §5.1 tier 4: the pages' head is a 4/8-bit affine
+ * group-quantised weight with per-group scales and biases).  Same contract as
+ * orpo_head_fwd / orpo_head_bwd with W replaced by:
+ *   wq      uint8 [V, d * bits / 8]: 4-bit values two per byte (even column in the
+ *           low nibble), or one 8-bit value per byte; 4-byte (4-bit) or 8-byte
+ *           (8-bit) aligned;
+ *   scales, biases  bf16 bit patterns [V, d / group];
+ *   bits    4 or 8;  group  a multiple of 8 that divides d.
+ * The head's weight is W[v, j] = bf16(scales[v, j/group] * q[v, j] + biases[v, j/group])
+ * (fp32 arithmetic, one nearest-even rounding).  Each call dequantises W one
+ * vocabulary block at a time into the workspace (bounded, at most 256 MiB of bf16)
+ * and runs the bf16 tensor-core path on it; nothing grows like V * d beyond the
+ * quantised weights themselves.  dW, when given, is the gradient with respect to
+ * the dequantised weight.  The workspace must hold orpo_head_q_workspace_bytes.
+ * Host errors: ORPO_ERR_ARG for bits / group, ORPO_ERR_ALIGN for wq alignment.
+ */
+size_t orpo_head_q_workspace_bytes(int64_t M, int64_t V, int64_t d);
+int orpo_head_fwd_q(const void* h_bf16, const uint8_t* wq, const void* scales_bf16,
+                    const void* biases_bf16, int bits, int group, const int32_t* targets,
+                    const uint8_t* mask, int64_t M, int64_t V, int64_t d, float softcap,
+                    float* logp, float* lse, void* workspace, size_t ws_bytes,
+                    int32_t* status, void* stream);
+int orpo_head_bwd_q(const void* h_bf16, const uint8_t* wq, const void* scales_bf16,
+                    const void* biases_bf16, int bits, int group, const int32_t* targets,
+                    const uint8_t* mask, const float* lse, const float* g, int64_t M,
+                    int64_t V, int64_t d, float softcap, float* dh, float* dW,
+                    int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* status,
+                    void* stream);
 
 /* Text of a return code or of a set of ORPO_STATUS_* bits (static storage). */
 const char* orpo_status_string(int code);

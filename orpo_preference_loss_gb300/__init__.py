@@ -20,7 +20,7 @@ __all__ = [
     "OrpoError", "load", "lib_path", "orpo_head_workspace_bytes", "orpo_head_fwd", "orpo_loss",
     "orpo_head_bwd", "orpo_status_string", "orpo_debug_gemm", "OrpoHead", "STATUS_BITS",
     "orpo_profile_start", "orpo_profile_stop", "orpo_head_fwd_static", "orpo_debug_wait_timeout",
-    "orpo_pref_loss", "PREF_KINDS",
+    "orpo_pref_loss", "PREF_KINDS", "orpo_head_q_workspace_bytes", "orpo_head_fwd_q", "orpo_head_bwd_q",
 ]
 
 STATUS_BITS = {"target": 1 << 4, "seqid": 1 << 5, "empty": 1 << 6, "nonfinite": 1 << 7, "timeout": 1 << 8}
@@ -63,6 +63,14 @@ def load():
     L.orpo_debug_gemm.restype = ctypes.c_int
     L.orpo_pref_loss.argtypes = [ctypes.c_int, vp, vp, vp, i64, i32, f32, f32, vp, vp, vp, vp, vp, vp]
     L.orpo_pref_loss.restype = ctypes.c_int
+    L.orpo_head_q_workspace_bytes.argtypes = [i64, i64, i64]
+    L.orpo_head_q_workspace_bytes.restype = sz
+    L.orpo_head_fwd_q.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, vp, vp, i64, i64, i64, f32, vp, vp, vp,
+                                  sz, vp, vp]
+    L.orpo_head_fwd_q.restype = ctypes.c_int
+    L.orpo_head_bwd_q.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, i64, i64, i64, f32, vp,
+                                  vp, ctypes.c_int, vp, sz, vp, vp]
+    L.orpo_head_bwd_q.restype = ctypes.c_int
     L.orpo_head_fwd_static.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp, vp, vp, vp]
     L.orpo_head_fwd_static.restype = ctypes.c_int
     L.orpo_debug_wait_timeout.argtypes = [vp, i64, vp]
@@ -198,12 +206,58 @@ def orpo_head_bwd(h, W, targets, mask, lse, g, softcap, dh, dW, accumulate_dW, w
     _dev(lse, "lse", (torch.float32,), (M,))
     _dev(g, "g", (torch.float32,), (M,))
     _dev(dh, "dh", (torch.float32,), (M, d))
-    _dev(dW, "dW", (torch.float32,), (V, d))
+    if dW is not None:
+        _dev(dW, "dW", (torch.float32,), (V, d))
     _dev(workspace, "workspace", (torch.uint8,))
     _dev(status, "status", (torch.int32,))
     _check(load().orpo_head_bwd(_ptr(h), _ptr(W), _ptr(targets), _ptr(mask), _ptr(lse), _ptr(g), M, V, d,
                                 float(softcap), _ptr(dh), _ptr(dW), 1 if accumulate_dW else 0, _ptr(workspace),
                                 workspace.numel(), _ptr(status), _stream(stream)), "orpo_head_bwd")
+
+
+def orpo_head_q_workspace_bytes(M: int, V: int, d: int) -> int:
+    return int(load().orpo_head_q_workspace_bytes(M, V, d))
+
+
+def _quant_args(wq, scales, biases, V, d, bits, group):
+    _dev(wq, "wq", (torch.uint8,), (V, d * bits // 8))
+    _dev(scales, "scales", BF16, (V, d // group))
+    _dev(biases, "biases", BF16, (V, d // group))
+
+
+def orpo_head_fwd_q(h, wq, scales, biases, bits, group, targets, mask, softcap, logp, lse, workspace, status,
+                    stream=None):
+    """orpo_head_fwd on an affine group-quantised head (wq, scales, biases)."""
+    M, d = h.shape
+    V = wq.shape[0]
+    _dev(h, "h", BF16)
+    _quant_args(wq, scales, biases, V, d, bits, group)
+    _dev(targets, "targets", (torch.int32,), (M,))
+    _dev(mask, "mask", (torch.uint8, torch.bool), (M,))
+    _dev(logp, "logp", (torch.float32,), (M,))
+    _dev(lse, "lse", (torch.float32,), (M,))
+    _dev(workspace, "workspace", (torch.uint8,))
+    _check(load().orpo_head_fwd_q(_ptr(h), _ptr(wq), _ptr(scales), _ptr(biases), int(bits), int(group), _ptr(targets),
+                                  _ptr(mask), M, V, d, float(softcap), _ptr(logp), _ptr(lse), _ptr(workspace),
+                                  workspace.numel(), _ptr(status), _stream(stream)), "orpo_head_fwd_q")
+
+
+def orpo_head_bwd_q(h, wq, scales, biases, bits, group, targets, mask, lse, g, softcap, dh, dW, accumulate_dW,
+                    workspace, status, stream=None):
+    """orpo_head_bwd on an affine group-quantised head; dW (optional) is w.r.t. the dequantised weight."""
+    M, d = h.shape
+    V = wq.shape[0]
+    _dev(h, "h", BF16)
+    _quant_args(wq, scales, biases, V, d, bits, group)
+    _dev(lse, "lse", (torch.float32,), (M,))
+    _dev(g, "g", (torch.float32,), (M,))
+    _dev(dh, "dh", (torch.float32,), (M, d))
+    if dW is not None:
+        _dev(dW, "dW", (torch.float32,), (V, d))
+    _check(load().orpo_head_bwd_q(_ptr(h), _ptr(wq), _ptr(scales), _ptr(biases), int(bits), int(group), _ptr(targets),
+                                  _ptr(mask), _ptr(lse), _ptr(g), M, V, d, float(softcap), _ptr(dh), _ptr(dW),
+                                  1 if accumulate_dW else 0, _ptr(workspace), workspace.numel(), _ptr(status),
+                                  _stream(stream)), "orpo_head_bwd_q")
 
 
 def orpo_debug_gemm(A, B, C, M, N, K, a_mn_major, b_mn_major, status, stream=None):
@@ -219,7 +273,7 @@ def orpo_debug_wait_timeout(status, limit_ns, stream=None):
     _check(load().orpo_debug_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)), "orpo_debug_wait_timeout")
 
 
-PROFILE_KINDS = 6
+PROFILE_KINDS = 7
 
 
 def orpo_profile_start():

@@ -78,9 +78,19 @@ BwdBlocks bwd_blocks(int64_t M, int64_t V) {
   return BwdBlocks{Mc, std::min(Vpad, vc)};
 }
 
-size_t partial_bytes(int64_t M) {
+// forward partials: (max, sum-exp) per row and vocabulary split
+size_t partial_bytes(int64_t M, int nsplit_max) {
   const int64_t Mpad = std::max<int64_t>(kBM, cdiv(M, kBM) * kBM);
-  return (size_t)2 * kNsplitMax * Mpad * sizeof(float);
+  return (size_t)2 * nsplit_max * Mpad * sizeof(float);
+}
+
+// quantised head: most splits over all dequantised blocks, and the bf16 block of W
+constexpr int kNsplitMaxQ = 256;
+constexpr int64_t kWBlockBudget = 256ll << 20;
+
+void* align_ws(void* ws) {
+  uintptr_t p = reinterpret_cast<uintptr_t>(ws);
+  return reinterpret_cast<void*>((p + 1023) & ~uintptr_t(1023));
 }
 
 // Row pitch of the dZ block in elements: 64 past the width, so that rows of the
@@ -92,6 +102,17 @@ size_t scratch_bytes(int64_t M, int64_t V) {
   const BwdBlocks b = bwd_blocks(M, V);
   return (size_t)b.Mc * scratch_pitch(b) * 2;
 }
+
+// Rows of W dequantised at a time: a multiple of the backward's vocabulary block (so the backward
+// reuses the same buffer block by block) within kWBlockBudget bytes of bf16, at least one block.
+int64_t wblock_rows(int64_t M, int64_t V, int64_t d) {
+  const BwdBlocks b = bwd_blocks(M, V);
+  const int64_t fit = kWBlockBudget / (2 * d);
+  const int64_t k = std::max<int64_t>(1, fit / b.Vc);
+  return std::min(cdiv(V, kBN) * kBN, k * b.Vc);
+}
+
+size_t wblock_bytes(int64_t M, int64_t V, int64_t d) { return (size_t)wblock_rows(M, V, d) * d * 2; }
 
 // Unit counters of the dh/dW GEMM launches (dynamic scheduling): a fixed ring of
 // kCounters slots; launch k uses slot k % kCounters and the ring is zeroed
@@ -148,55 +169,238 @@ bool encode_map_mn3d(CUtensorMap* map, const void* base, uint64_t mn, uint64_t k
 
 using namespace orpo;
 
-extern "C" {
+// ---------------------------------------------------------------- forward / backward implementations
 
-size_t orpo_head_workspace_bytes(int64_t M, int64_t V, int64_t d) {
-  if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return 0;
-  return std::max(partial_bytes(M), scratch_bytes(M, V) + kCounterBytes) + 1024;
+// Source of an affine group-quantised head (nullptr: W is bf16).
+struct QuantW {
+  const uint8_t* wq;
+  const void* scales;
+  const void* biases;
+  int bits, group;
+};
+
+int check_quant(const QuantW* q, int64_t d) {
+  if (!q) return ORPO_OK;
+  if (!q->wq || !q->scales || !q->biases) return ORPO_ERR_NULL;
+  if ((q->bits != 4 && q->bits != 8) || q->group < 8 || q->group % 8 != 0 || d % q->group != 0)
+    return ORPO_ERR_ARG;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(q->wq);
+  if ((q->bits == 4 && (a & 3u)) || (q->bits == 8 && (a & 7u)) || (reinterpret_cast<uintptr_t>(q->scales) & 1u) ||
+      (reinterpret_cast<uintptr_t>(q->biases) & 1u))
+    return ORPO_ERR_ALIGN;
+  return ORPO_OK;
 }
 
-static void* align_ws(void* ws) {
-  uintptr_t p = reinterpret_cast<uintptr_t>(ws);
+// workspace layout (quantised path): [partials | S + counters] then the bf16 W block
+void* wblock_ptr(void* workspace, int64_t M, int64_t V) {
+  uintptr_t p = reinterpret_cast<uintptr_t>(align_ws(workspace));
+  p += std::max(partial_bytes(M, kNsplitMaxQ), scratch_bytes(M, V) + kCounterBytes);
   return reinterpret_cast<void*>((p + 1023) & ~uintptr_t(1023));
 }
 
-int orpo_head_fwd(const void* h, const void* W, const int32_t* targets, const uint8_t* mask, int64_t M, int64_t V,
-                  int64_t d, float softcap, float* logp, float* lse, void* workspace, size_t ws_bytes,
-                  int32_t* status, void* stream) {
+int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* targets, const uint8_t* mask,
+                  int64_t M, int64_t V, int64_t d, float softcap, float* logp, float* lse, void* workspace,
+                  size_t ws_bytes, int32_t* status, void* stream) {
   if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return ORPO_ERR_SHAPE;
   if (M == 0) return ORPO_OK;
-  if (!h || !W || !targets || !mask || !logp || !lse || !workspace || !status) return ORPO_ERR_NULL;
-  if (d % 8 != 0 || !aligned16(h) || !aligned16(W) || !aligned16(workspace)) return ORPO_ERR_ALIGN;
+  if (!h || (!W && !q) || !targets || !mask || !logp || !lse || !workspace || !status) return ORPO_ERR_NULL;
+  if (d % 8 != 0 || !aligned16(h) || (W && !aligned16(W)) || !aligned16(workspace)) return ORPO_ERR_ALIGN;
+  if (int e = check_quant(q, d)) return e;
   if (!isfinite(softcap)) return ORPO_ERR_ARG;
-  if (ws_bytes < orpo_head_workspace_bytes(M, V, d)) return ORPO_ERR_WORKSPACE;
+  if (ws_bytes < (q ? orpo_head_q_workspace_bytes(M, V, d) : orpo_head_workspace_bytes(M, V, d)))
+    return ORPO_ERR_WORKSPACE;
   int sms = 0;
   if (int e = device_check(&sms)) return e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   FwdLaunch L;
-  const int64_t n_mt = cdiv(M, kBM), n_vt = cdiv(V, kBN);
-  if (!encode_map_2d(&L.mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, kBM) ||
-      !encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, kBN))
-    return ORPO_ERR_CUDA;
+  const int64_t n_mt = cdiv(M, kBM);
+  const int64_t Mpad = n_mt * kBM;
+  const int nsplit_max = q ? kNsplitMaxQ : kNsplitMax;
+  float* base = reinterpret_cast<float*>(align_ws(workspace));
+  if (!encode_map_2d(&L.mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, kBM)) return ORPO_ERR_CUDA;
   L.n_mt = (int)n_mt;
-  L.n_vt = (int)n_vt;
-  L.nsplit = choose_nsplit(n_mt, n_vt, sms);
   L.kblocks = (int)cdiv(d, 64);
   L.targets = targets;
   L.mask = mask;
   L.logp = logp;
   L.lse = lse;
-  const int64_t Mpad = n_mt * kBM;
-  float* base = reinterpret_cast<float*>(align_ws(workspace));
   L.part_m = base;
-  L.part_s = base + (size_t)kNsplitMax * Mpad;
+  L.part_s = base + (size_t)nsplit_max * Mpad;
   L.M = (int)M;
   L.Mpad = (int)Mpad;
   L.V = (int)V;
   L.softcap = softcap > 0.f ? softcap : 0.f;
   L.status = status;
-  L.grid = (int)std::min<int64_t>(n_mt * L.nsplit, sms);
-  return launch_forward(L, st) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
+  // vocabulary blocks: the whole vocabulary for bf16 W; bounded dequantised blocks otherwise
+  const int64_t vb = q ? wblock_rows(M, V, d) : V;
+  const int64_t nblocks = cdiv(V, vb);
+  const int per_block = std::max<int>(1, nsplit_max / (int)nblocks);
+  void* Wb = q ? wblock_ptr(workspace, M, V) : nullptr;
+  int split0 = 0;
+  for (int64_t v0 = 0; v0 < V; v0 += vb) {
+    const int64_t vc = std::min(vb, V - v0);
+    const int64_t n_vt = cdiv(vc, kBN);
+    if (q) {
+      if (launch_dequant(q->wq, q->scales, q->biases, q->bits, q->group, v0, vc, d, Wb, st) != cudaSuccess)
+        return ORPO_ERR_CUDA;
+      if (!encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Wb, d, vc, d * 2, 64, kBN)) return ORPO_ERR_CUDA;
+    } else if (!encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, kBN)) {
+      return ORPO_ERR_CUDA;
+    }
+    L.n_vt = (int)n_vt;
+    L.nsplit = std::min<int>(choose_nsplit(n_mt, n_vt, sms), per_block);
+    L.col0 = (int)v0;
+    L.split0 = split0;
+    L.grid = (int)std::min<int64_t>(n_mt * L.nsplit, sms);
+    if (launch_forward_logits(L, st) != cudaSuccess) return ORPO_ERR_CUDA;
+    split0 += L.nsplit;
+  }
+  return launch_forward_merge(L, split0, st) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
+}
+
+int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* targets, const uint8_t* mask,
+                  const float* lse, const float* g, int64_t M, int64_t V, int64_t d, float softcap, float* dh,
+                  float* dW, int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
+  if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return ORPO_ERR_SHAPE;
+  if ((!W && !q) || !status) return ORPO_ERR_NULL;
+  if (M > 0 && (!h || !targets || !mask || !lse || !g || !dh || !workspace)) return ORPO_ERR_NULL;
+  if (d % 8 != 0 || (W && !aligned16(W)) || (dW && !aligned16(dW)) ||
+      (M > 0 && (!aligned16(h) || !aligned16(dh) || !aligned16(workspace))))
+    return ORPO_ERR_ALIGN;
+  if (int e = check_quant(q, d)) return e;
+  if (!isfinite(softcap)) return ORPO_ERR_ARG;
+  if (M > 0 && ws_bytes < (q ? orpo_head_q_workspace_bytes(M, V, d) : orpo_head_workspace_bytes(M, V, d)))
+    return ORPO_ERR_WORKSPACE;
+  int sms = 0;
+  if (int e = device_check(&sms)) return e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    if (!dW || accumulate_dW) return ORPO_OK;
+    return cudaMemsetAsync(dW, 0, (size_t)V * d * sizeof(float), st) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
+  }
+
+  const BwdBlocks B = bwd_blocks(M, V);
+  void* S = align_ws(workspace);
+  int* counters = reinterpret_cast<int*>(static_cast<uint8_t*>(S) + scratch_bytes(M, V));
+  void* Wb = q ? wblock_ptr(workspace, M, V) : nullptr;
+  int64_t launch = 0;
+  const int64_t sp = scratch_pitch(B);
+  const bool d64 = d % 64 == 0;  // MN-major h / W fetched with one 3-D box per stage
+  RecLaunch R;
+  GemmLaunch G;
+  bool ok = encode_map_2d(&R.mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, kBM) &&
+            encode_map_2d(&R.ms_store, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, sp * 2, 64, 32) &&
+            // gemm maps: 0 S K-major rows, 1 W MN-major, 2 S MN-major, 3 h MN-major, 4 dh, 5 dW
+            encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, sp * 2, 64, kBM) &&
+            encode_map_mn3d(&G.maps[2], S, B.Vc, B.Mc, sp * 2, kBM / 64) &&
+            (d64 ? encode_map_mn3d(&G.maps[3], h, d, M, d * 2, kBN / 64)
+                 : encode_map_2d(&G.maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, 64)) &&
+            encode_map_2d(&G.maps[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dh, d, M, d * 4, 32, 32) &&
+            (!dW || encode_map_2d(&G.maps[5], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, d, V, d * 4, 32, 32));
+  if (!ok) return ORPO_ERR_CUDA;
+  if (!dW) G.maps[5] = G.maps[4];
+  // W maps over the whole bf16 head (encoded once), or per block over the dequantised copy
+  auto encode_w = [&](const void* base, int64_t rows) {
+    return encode_map_2d(&R.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d, rows, d * 2, 64, kBN) &&
+           (d64 ? encode_map_mn3d(&G.maps[1], base, d, rows, d * 2, kBN / 64)
+                : encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d, rows, d * 2, 64, 64));
+  };
+  if (!q && !encode_w(W, V)) return ORPO_ERR_CUDA;
+  G.status = status;
+  R.targets = targets;
+  R.mask = mask;
+  R.lse = lse;
+  R.g = g;
+  R.M = (int)M;
+  R.V = (int)V;
+  R.softcap = softcap > 0.f ? softcap : 0.f;
+  R.status = status;
+  R.kblocks = (int)cdiv(d, 64);
+  const int n_nt = (int)cdiv(d, kBN);
+
+  for (int64_t v0 = 0, vblock = 0; v0 < V; v0 += B.Vc, ++vblock) {
+    const int64_t vc = std::min(B.Vc, V - v0);
+    if (q) {
+      if (launch_dequant(q->wq, q->scales, q->biases, q->bits, q->group, v0, vc, d, Wb, st) != cudaSuccess ||
+          !encode_w(Wb, vc))
+        return ORPO_ERR_CUDA;
+    }
+    for (int64_t m0 = 0; m0 < M; m0 += B.Mc) {
+      const int64_t mc = std::min(B.Mc, M - m0);
+      const int n_mt = (int)cdiv(mc, kBM);
+      const int n_vt = (int)cdiv(vc, kBN);
+      R.m0 = (int)m0;
+      R.v0 = (int)v0;
+      R.w_row0 = q ? 0 : (int)v0;
+      R.n_mt = n_mt;
+      R.n_vt = n_vt;
+      R.grid = (int)std::min<int64_t>((int64_t)n_mt * n_vt, sms);
+      if (launch_recompute(R, st) != cudaSuccess) return ORPO_ERR_CUDA;
+
+      GemmClassH cdw{};  // dW[v0 + ..] (+)= S^T h[m0 + ..]
+      if (dW) {
+        cdw.a_map = 2, cdw.a_mn = 2, cdw.a_mn_base = 0, cdw.a_k_base = 0;
+        cdw.b_map = 3, cdw.b_mn = d64 ? 2 : 1, cdw.b_mn_base = 0, cdw.b_k_base = (int)m0;
+        cdw.out_map = 5, cdw.out_row_base = (int)v0, cdw.out_col_base = 0;
+        cdw.reduce = (m0 > 0 || accumulate_dW) ? 1 : 0;
+        cdw.out_rows = (int)V, cdw.out_cols = (int)d;
+        cdw.n_mt = (int)cdiv(vc, kBM), cdw.n_nt = n_nt, cdw.kblocks = (int)cdiv(mc, 64);
+        cdw.mt_major = 1;  // CTAs running together share one column slab of S; h stays in L2
+      }
+      GemmClassH cdh{};  // dh[m0 + ..] (+)= S W[v0 + ..]
+      cdh.a_map = 0, cdh.a_mn = 0, cdh.a_mn_base = 0, cdh.a_k_base = 0;
+      cdh.b_map = 1, cdh.b_mn = d64 ? 2 : 1, cdh.b_mn_base = 0, cdh.b_k_base = q ? 0 : (int)v0;
+      cdh.out_map = 4, cdh.out_row_base = (int)m0, cdh.out_col_base = 0;
+      cdh.reduce = vblock > 0 ? 1 : 0;
+      cdh.out_rows = (int)M, cdh.out_cols = (int)d;
+      cdh.n_mt = n_mt, cdh.n_nt = n_nt, cdh.kblocks = (int)cdiv(vc, 64);
+      cdh.mt_major = 1;
+      // longer tiles first
+      if (dW && cdw.kblocks >= cdh.kblocks) {
+        G.cls[0] = cdw;
+        G.cls[1] = cdh;
+      } else {
+        G.cls[0] = cdh;
+        G.cls[1] = cdw;
+      }
+      const int64_t units = (int64_t)cdw.n_mt * cdw.n_nt + (int64_t)cdh.n_mt * cdh.n_nt;
+      G.grid = (int)std::min<int64_t>(units, sms);
+      if (launch % kCounters == 0 && cudaMemsetAsync(counters, 0, kCounterBytes, st) != cudaSuccess)
+        return ORPO_ERR_CUDA;
+      G.counter = counters + (launch++ % kCounters);
+      if (launch_gemm(G, st, K_GEMM) != cudaSuccess) return ORPO_ERR_CUDA;
+    }
+  }
+  return ORPO_OK;
+}
+
+extern "C" {
+
+size_t orpo_head_workspace_bytes(int64_t M, int64_t V, int64_t d) {
+  if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return 0;
+  return std::max(partial_bytes(M, kNsplitMax), scratch_bytes(M, V) + kCounterBytes) + 1024;
+}
+
+size_t orpo_head_q_workspace_bytes(int64_t M, int64_t V, int64_t d) {
+  if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return 0;
+  return std::max(partial_bytes(M, kNsplitMaxQ), scratch_bytes(M, V) + kCounterBytes) + wblock_bytes(M, V, d) +
+         2048;
+}
+
+int orpo_head_fwd(const void* h, const void* W, const int32_t* targets, const uint8_t* mask, int64_t M, int64_t V,
+                  int64_t d, float softcap, float* logp, float* lse, void* workspace, size_t ws_bytes,
+                  int32_t* status, void* stream) {
+  return head_fwd_impl(h, W, nullptr, targets, mask, M, V, d, softcap, logp, lse, workspace, ws_bytes, status,
+                       stream);
+}
+
+int orpo_head_fwd_q(const void* h, const uint8_t* wq, const void* scales, const void* biases, int bits, int group,
+                    const int32_t* targets, const uint8_t* mask, int64_t M, int64_t V, int64_t d, float softcap,
+                    float* logp, float* lse, void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
+  const QuantW q{wq, scales, biases, bits, group};
+  return head_fwd_impl(h, nullptr, &q, targets, mask, M, V, d, softcap, logp, lse, workspace, ws_bytes, status,
+                       stream);
 }
 
 int orpo_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int64_t M, int32_t n_pairs,
@@ -235,101 +439,17 @@ int orpo_pref_loss(int kind, const float* logp, const int32_t* seq_id, const uin
 int orpo_head_bwd(const void* h, const void* W, const int32_t* targets, const uint8_t* mask, const float* lse,
                   const float* g, int64_t M, int64_t V, int64_t d, float softcap, float* dh, float* dW,
                   int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
-  if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return ORPO_ERR_SHAPE;
-  if (!W || !dW || !status) return ORPO_ERR_NULL;
-  if (M > 0 && (!h || !targets || !mask || !lse || !g || !dh || !workspace)) return ORPO_ERR_NULL;
-  if (d % 8 != 0 || !aligned16(W) || !aligned16(dW) || (M > 0 && (!aligned16(h) || !aligned16(dh) ||
-                                                                  !aligned16(workspace))))
-    return ORPO_ERR_ALIGN;
-  if (!isfinite(softcap)) return ORPO_ERR_ARG;
-  if (M > 0 && ws_bytes < orpo_head_workspace_bytes(M, V, d)) return ORPO_ERR_WORKSPACE;
-  int sms = 0;
-  if (int e = device_check(&sms)) return e;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (M == 0) {
-    if (accumulate_dW) return ORPO_OK;
-    return cudaMemsetAsync(dW, 0, (size_t)V * d * sizeof(float), st) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
-  }
+  return head_bwd_impl(h, W, nullptr, targets, mask, lse, g, M, V, d, softcap, dh, dW, accumulate_dW, workspace,
+                       ws_bytes, status, stream);
+}
 
-  const BwdBlocks B = bwd_blocks(M, V);
-  void* S = align_ws(workspace);
-  int* counters = reinterpret_cast<int*>(static_cast<uint8_t*>(S) + scratch_bytes(M, V));
-  int64_t launch = 0;
-  const int64_t sp = scratch_pitch(B);
-  const bool d64 = d % 64 == 0;  // MN-major h / W fetched with one 3-D box per stage
-  RecLaunch R;
-  GemmLaunch G;
-  bool ok = encode_map_2d(&R.mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, kBM) &&
-            encode_map_2d(&R.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, kBN) &&
-            encode_map_2d(&R.ms_store, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, sp * 2, 64, 32) &&
-            // gemm maps: 0 S K-major rows, 1 W MN-major, 2 S MN-major, 3 h MN-major, 4 dh, 5 dW
-            encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, sp * 2, 64, kBM) &&
-            (d64 ? encode_map_mn3d(&G.maps[1], W, d, V, d * 2, kBN / 64)
-                 : encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, 64)) &&
-            encode_map_mn3d(&G.maps[2], S, B.Vc, B.Mc, sp * 2, kBM / 64) &&
-            (d64 ? encode_map_mn3d(&G.maps[3], h, d, M, d * 2, kBN / 64)
-                 : encode_map_2d(&G.maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, 64)) &&
-            encode_map_2d(&G.maps[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dh, d, M, d * 4, 32, 32) &&
-            encode_map_2d(&G.maps[5], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, d, V, d * 4, 32, 32);
-  if (!ok) return ORPO_ERR_CUDA;
-  G.status = status;
-  R.targets = targets;
-  R.mask = mask;
-  R.lse = lse;
-  R.g = g;
-  R.M = (int)M;
-  R.V = (int)V;
-  R.softcap = softcap > 0.f ? softcap : 0.f;
-  R.status = status;
-  R.kblocks = (int)cdiv(d, 64);
-  const int n_nt = (int)cdiv(d, kBN);
-
-  for (int64_t m0 = 0; m0 < M; m0 += B.Mc) {
-    const int64_t mc = std::min(B.Mc, M - m0);
-    const int n_mt = (int)cdiv(mc, kBM);
-    for (int64_t v0 = 0; v0 < V; v0 += B.Vc) {
-      const int64_t vc = std::min(B.Vc, V - v0);
-      const int n_vt = (int)cdiv(vc, kBN);
-      R.m0 = (int)m0;
-      R.v0 = (int)v0;
-      R.n_mt = n_mt;
-      R.n_vt = n_vt;
-      R.grid = (int)std::min<int64_t>((int64_t)n_mt * n_vt, sms);
-      if (launch_recompute(R, st) != cudaSuccess) return ORPO_ERR_CUDA;
-
-      GemmClassH cdw{};  // dW[v0 + ..] (+)= S^T h[m0 + ..]
-      cdw.a_map = 2, cdw.a_mn = 2, cdw.a_mn_base = 0, cdw.a_k_base = 0;
-      cdw.b_map = 3, cdw.b_mn = d64 ? 2 : 1, cdw.b_mn_base = 0, cdw.b_k_base = (int)m0;
-      cdw.out_map = 5, cdw.out_row_base = (int)v0, cdw.out_col_base = 0;
-      cdw.reduce = (m0 > 0 || accumulate_dW) ? 1 : 0;
-      cdw.out_rows = (int)V, cdw.out_cols = (int)d;
-      cdw.n_mt = (int)cdiv(vc, kBM), cdw.n_nt = n_nt, cdw.kblocks = (int)cdiv(mc, 64);
-      cdw.mt_major = 1;  // CTAs running together share one column slab of S; h stays in L2
-      GemmClassH cdh{};  // dh[m0 + ..] (+)= S W[v0 + ..]
-      cdh.a_map = 0, cdh.a_mn = 0, cdh.a_mn_base = 0, cdh.a_k_base = 0;
-      cdh.b_map = 1, cdh.b_mn = d64 ? 2 : 1, cdh.b_mn_base = 0, cdh.b_k_base = (int)v0;
-      cdh.out_map = 4, cdh.out_row_base = (int)m0, cdh.out_col_base = 0;
-      cdh.reduce = v0 > 0 ? 1 : 0;
-      cdh.out_rows = (int)M, cdh.out_cols = (int)d;
-      cdh.n_mt = n_mt, cdh.n_nt = n_nt, cdh.kblocks = (int)cdiv(vc, 64);
-      cdh.mt_major = 1;
-      // longer tiles first
-      if (cdw.kblocks >= cdh.kblocks) {
-        G.cls[0] = cdw;
-        G.cls[1] = cdh;
-      } else {
-        G.cls[0] = cdh;
-        G.cls[1] = cdw;
-      }
-      const int64_t units = (int64_t)cdw.n_mt * cdw.n_nt + (int64_t)cdh.n_mt * cdh.n_nt;
-      G.grid = (int)std::min<int64_t>(units, sms);
-      if (launch % kCounters == 0 && cudaMemsetAsync(counters, 0, kCounterBytes, st) != cudaSuccess)
-        return ORPO_ERR_CUDA;
-      G.counter = counters + (launch++ % kCounters);
-      if (launch_gemm(G, st, K_GEMM) != cudaSuccess) return ORPO_ERR_CUDA;
-    }
-  }
-  return ORPO_OK;
+int orpo_head_bwd_q(const void* h, const uint8_t* wq, const void* scales, const void* biases, int bits, int group,
+                    const int32_t* targets, const uint8_t* mask, const float* lse, const float* g, int64_t M,
+                    int64_t V, int64_t d, float softcap, float* dh, float* dW, int accumulate_dW, void* workspace,
+                    size_t ws_bytes, int32_t* status, void* stream) {
+  const QuantW q{wq, scales, biases, bits, group};
+  return head_bwd_impl(h, nullptr, &q, targets, mask, lse, g, M, V, d, softcap, dh, dW, accumulate_dW, workspace,
+                       ws_bytes, status, stream);
 }
 
 int orpo_debug_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int a_mn_major,

@@ -25,13 +25,14 @@ struct RecSched {
   const CUtensorMap* mh;
   const CUtensorMap* mw;
   int m0, v0, n_mt, n_vt, kblocks;
+  int w_row0;  // row of the W map that holds vocabulary column v0
   __device__ int num_units() const { return n_mt * n_vt; }
   __device__ int unit_len(int) const { return 1; }
   __device__ TileOps tile(int u, int) const {
     const int vt = u / n_mt, mt = u - vt * n_mt;
     TileOps t;
     t.a = Operand{mh, 0, m0 + mt * BM, 0};
-    t.b = Operand{mw, 0, v0 + vt * BN, 0};
+    t.b = Operand{mw, 0, w_row0 + vt * BN, 0};
     t.kblocks = kblocks;
     return t;
   }
@@ -334,7 +335,7 @@ cudaError_t launch_rec_kernel(const RecLaunch& L, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
-  RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks};
+  RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks, L.w_row0};
   RecArgs a{L.targets, L.mask, L.lse, L.g, L.M, L.V, L.softcap, L.status};
   prof_begin(K_REC, st);
   rec_kernel<cap><<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, L.ms_store, sched, a);

@@ -51,6 +51,8 @@ struct FwdArgs {
   int M, Mpad, V;
   float softcap;
   int32_t* status;
+  int col0;    // vocabulary column of row 0 of the W map (0 unless W is a block of the vocabulary)
+  int split0;  // index of this launch's first split in the partial arrays
 };
 
 // Per-row online softmax state of one epilogue thread, base-2 units.
@@ -164,7 +166,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int j = 0; j < len; ++j, ++tcount) {
         uint32_t taddr;
         if (!epi_acquire(ctl, tmem_base, tcount, warp, p.status, &taddr)) return;
-        const int col_base = (vt0 + j) * BN;
+        const int col_base = p.col0 + (vt0 + j) * BN;
         uint32_t ra[32], rb[32];
         tmem_ld32(taddr, ra);
 #pragma unroll 1
@@ -178,8 +180,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         epi_release(ctl, tcount);
       }
-      p.part_m[(size_t)s * p.Mpad + row] = st.m;
-      p.part_s[(size_t)s * p.Mpad + row] = st.s;
+      p.part_m[(size_t)(p.split0 + s) * p.Mpad + row] = st.m;
+      p.part_s[(size_t)(p.split0 + s) * p.Mpad + row] = st.s;
     }
   });
 }
@@ -222,7 +224,7 @@ cudaError_t launch_fwd_kernel(const FwdLaunch& L, cudaStream_t st) {
     attr_set[dev] = 1;
   }
   FwdSched sched{nullptr, nullptr, L.n_mt, L.nsplit, L.n_vt, L.kblocks};
-  FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M, L.Mpad, L.V, L.softcap, L.status};
+  FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M, L.Mpad, L.V, L.softcap, L.status, L.col0, L.split0};
   prof_begin(K_FWD, st);
   fwd_kernel<cap><<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, sched, a);
   prof_end(K_FWD, st);
@@ -231,18 +233,26 @@ cudaError_t launch_fwd_kernel(const FwdLaunch& L, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st) {
+cudaError_t launch_forward_logits(const FwdLaunch& L, cudaStream_t st) {
   const int cap = L.softcap > 0.f ? (L.softcap <= kCapExpMax ? kCapExp : kCapHybrid) : kCapOff;
-  cudaError_t e = cap == kCapExp      ? launch_fwd_kernel<kCapExp>(L, st)
-                  : cap == kCapHybrid ? launch_fwd_kernel<kCapHybrid>(L, st)
-                                      : launch_fwd_kernel<kCapOff>(L, st);
-  if (e != cudaSuccess) return e;
+  return cap == kCapExp      ? launch_fwd_kernel<kCapExp>(L, st)
+         : cap == kCapHybrid ? launch_fwd_kernel<kCapHybrid>(L, st)
+                             : launch_fwd_kernel<kCapOff>(L, st);
+}
+
+cudaError_t launch_forward_merge(const FwdLaunch& L, int nsplit_total, cudaStream_t st) {
   const int threads = 256;
   prof_begin(K_MERGE, st);
-  merge_kernel<<<(L.M + threads - 1) / threads, threads, 0, st>>>(L.part_m, L.part_s, L.nsplit, L.Mpad, L.M, L.V,
+  merge_kernel<<<(L.M + threads - 1) / threads, threads, 0, st>>>(L.part_m, L.part_s, nsplit_total, L.Mpad, L.M, L.V,
                                                                   L.targets, L.mask, L.logp, L.lse, L.status);
   prof_end(K_MERGE, st);
   return cudaGetLastError();
+}
+
+cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st) {
+  cudaError_t e = launch_forward_logits(L, st);
+  if (e != cudaSuccess) return e;
+  return launch_forward_merge(L, L.nsplit, st);
 }
 
 }  // namespace orpo

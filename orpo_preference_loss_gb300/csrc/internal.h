@@ -8,7 +8,7 @@
 namespace orpo {
 
 // ---- launch timing (profile.cu); no-ops unless orpo_profile_start() was called
-enum KernelKind { K_FWD = 0, K_MERGE, K_LOSS, K_REC, K_GEMM, K_DEBUG, K_NKINDS };
+enum KernelKind { K_FWD = 0, K_MERGE, K_LOSS, K_REC, K_GEMM, K_DEBUG, K_DEQUANT, K_NKINDS };
 void prof_begin(int kind, cudaStream_t st);
 void prof_end(int kind, cudaStream_t st);
 
@@ -33,8 +33,12 @@ struct FwdLaunch {
   float softcap;
   int32_t* status;
   int grid;
+  int col0 = 0;    // vocabulary column of row 0 of mw
+  int split0 = 0;  // first split index this launch writes
 };
-cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st);
+cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st);  // logits kernel + merge of L.nsplit splits
+cudaError_t launch_forward_logits(const FwdLaunch& L, cudaStream_t st);
+cudaError_t launch_forward_merge(const FwdLaunch& L, int nsplit_total, cudaStream_t st);
 
 // ---- backward: recompute dZ for one (row block, vocab block) into the scratch
 struct RecLaunch {
@@ -48,8 +52,13 @@ struct RecLaunch {
   float softcap;
   int32_t* status;
   int grid;
+  int w_row0;  // row of mw holding vocabulary column m0's block start v0 (v0 itself unless W is a block copy)
 };
 cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st);
+
+// ---- quantised head: affine group dequantisation of W rows [v0, v0 + rows) into bf16 [rows, d]
+cudaError_t launch_dequant(const uint8_t* wq, const void* scales, const void* biases, int bits, int group,
+                           int64_t v0, int64_t rows, int64_t d, void* out_bf16, cudaStream_t st);
 
 // ---- generic two-class GEMM with an fp32 store / reduce-add epilogue
 struct GemmClassH {
