@@ -67,3 +67,29 @@ def test_backward_restricted_support(full):
     other = np.ones(w.M, dtype=bool)
     other[rows] = False
     assert np.all(dh[other] == 0)
+
+
+@pytest.mark.parametrize("d", [1600, 1544])
+def test_multiblock_ragged_vocab_and_hidden(d):
+    """M 20000 (two row blocks), V 50257 (seven vocabulary blocks, ragged tail); d 1544 is not a
+    multiple of 64, so the MN-major operands take the 2-D-box path."""
+    w = workloads.make("small", M=20000, d=d, V=50257)
+    t = to_dev(w)
+    W64 = f64(w.W)
+    rng = np.random.default_rng(31)
+    rows = np.unique(np.concatenate([[0, w.M - 1, 16383, 16384], rng.choice(w.M, 36, replace=False)]))
+    logp, lse, st = gpu_forward(t, w.M, w.V, w.d, 0.0)
+    assert st == 0
+    rl, rs = oracle.head_forward(f64(w.h[rows]), W64, w.targets[rows], w.mask[rows], 0.0)
+    assert np.max(np.abs(lse[rows] - rs)) < LOGP_ATOL and np.max(np.abs(logp[rows] - rl)) < LOGP_ATOL
+    g = np.zeros(w.M, dtype=np.float32)
+    g[rows] = (rng.standard_normal(len(rows)) * 1e-3).astype(np.float32)
+    lse_in = np.zeros(w.M, dtype=np.float32)
+    lse_in[rows] = rs.astype(np.float32)
+    dh, dW, st = gpu_backward(t, lse_in, g, w.M, w.V, w.d, 0.0)
+    assert st == 0
+    rdh_rows, rdW = oracle.head_backward(f64(w.h[rows]), W64, w.targets[rows], w.mask[rows], lse_in[rows], g[rows],
+                                         0.0)
+    rdh = np.zeros((w.M, w.d))
+    rdh[rows] = rdh_rows
+    assert relfro(dh, rdh) < GRAD_RELFRO and relfro(dW, rdW) < GRAD_RELFRO
