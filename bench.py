@@ -255,8 +255,6 @@ def ours(args, w, rank, world, local):
         host["qs"] = torch.from_numpy(qs.view(np.int16)).pin_memory()
         host["qb"] = torch.from_numpy(qb.view(np.int16)).pin_memory()
     t = {k: v.to(dev) for k, v in host.items()}
-    h_bf = t["h"].view(torch.bfloat16)
-    W_bf = None if args.quant else t["W"].view(torch.bfloat16)
     logp = torch.empty(M, dtype=torch.float32, device=dev)
     lse = torch.empty(M, dtype=torch.float32, device=dev)
     out = torch.empty(5, dtype=torch.float32, device=dev)
@@ -274,22 +272,29 @@ def ours(args, w, rank, world, local):
     torch.cuda.reset_peak_memory_stats(dev)
     ws_bytes = orpo.orpo_head_q_workspace_bytes(M, V, d) if args.quant else orpo.orpo_head_workspace_bytes(M, V, d)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    if args.quant:
-        qw = (t["wq"], t["qs"].view(torch.bfloat16), t["qb"].view(torch.bfloat16), args.quant, 64)
 
-    def step():
+    def views(inp):
+        """Device views of one input set: h (bf16), W (bf16) or its quantised parts."""
+        hv = inp["h"].view(torch.bfloat16)
         if args.quant:
-            orpo.orpo_head_fwd_q(h_bf, *qw, t["targets"], t["mask"], w.softcap, logp, lse, ws, status)
+            return hv, (inp["wq"], inp["qs"].view(torch.bfloat16), inp["qb"].view(torch.bfloat16), args.quant, 64)
+        return hv, inp["W"].view(torch.bfloat16)
+
+    def step(inp=None):
+        inp = t if inp is None else inp
+        hv, wv = views(inp)
+        if args.quant:
+            orpo.orpo_head_fwd_q(hv, *wv, inp["targets"], inp["mask"], w.softcap, logp, lse, ws, status)
         else:
-            orpo.orpo_head_fwd(h_bf, W_bf, t["targets"], t["mask"], w.softcap, logp, lse, ws, status)
+            orpo.orpo_head_fwd(hv, wv, inp["targets"], inp["mask"], w.softcap, logp, lse, ws, status)
         if args.loss == "orpo":
-            orpo.orpo_loss(logp, t["seq_id"], t["mask"], P, w.lam, out, ell, g, status)
+            orpo.orpo_loss(logp, inp["seq_id"], inp["mask"], P, w.lam, out, ell, g, status)
         else:
-            orpo.orpo_pref_loss(args.loss, logp, t["seq_id"], t["mask"], P, beta, 0.5, ref, out, ell, g, status)
+            orpo.orpo_pref_loss(args.loss, logp, inp["seq_id"], inp["mask"], P, beta, 0.5, ref, out, ell, g, status)
         if args.quant:
-            orpo.orpo_head_bwd_q(h_bf, *qw, t["targets"], t["mask"], lse, g, w.softcap, dh, dW, False, ws, status)
+            orpo.orpo_head_bwd_q(hv, *wv, inp["targets"], inp["mask"], lse, g, w.softcap, dh, dW, False, ws, status)
         else:
-            orpo.orpo_head_bwd(h_bf, W_bf, t["targets"], t["mask"], lse, g, w.softcap, dh, dW, False, ws, status)
+            orpo.orpo_head_bwd(hv, wv, inp["targets"], inp["mask"], lse, g, w.softcap, dh, dW, False, ws, status)
 
     for _ in range(args.warmup):
         step()
@@ -326,20 +331,40 @@ def ours(args, w, rank, world, local):
     ms_step = ms / args.steps
     value = world * M * args.steps / (ms / 1e3)
 
-    # ---- end to end through host buffers: H2D inputs, step, D2H loss/metrics
+    # ---- end to end through host buffers: every step copies its inputs from pinned host memory
+    # and reads its loss / metrics back.  Two device input sets and a copy stream let the copy of
+    # step k + 1's inputs run while step k computes; step k waits for its own copy.
     e2e = None
     if not args.no_e2e:
         out_host = torch.empty(5, dtype=torch.float32).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         d2h = out_host.numel() * out_host.element_size()
+        sets = [{k: torch.empty_like(v) for k, v in t.items()} for _ in range(2)]
+        copy_stream = torch.cuda.Stream(dev)
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        freed = [torch.cuda.Event(), torch.cuda.Event()]
+
+        def issue_copy(k):
+            b = k % 2
+            with torch.cuda.stream(copy_stream):
+                if k >= 2:
+                    copy_stream.wait_event(freed[b])   # step k - 2 is done with this set
+                for name in host:
+                    sets[b][name].copy_(host[name], non_blocking=True)
+                copied[b].record(copy_stream)
+
         barrier()
         torch.cuda.synchronize()
         e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e2.record(stream)
-        for _ in range(args.steps):
-            for k in host:
-                t[k].copy_(host[k], non_blocking=True)
-            step()
+        copy_stream.wait_event(e2)
+        issue_copy(0)
+        for k in range(args.steps):
+            if k + 1 < args.steps:
+                issue_copy(k + 1)
+            stream.wait_event(copied[k % 2])
+            step(sets[k % 2])
+            freed[k % 2].record(stream)
             out_host.copy_(out, non_blocking=True)
         e3.record(stream)
         torch.cuda.synchronize()
@@ -349,7 +374,8 @@ def ours(args, w, rank, world, local):
             dist.all_reduce(x, op=dist.ReduceOp.MAX)
             ms2 = float(x.item())
         e2e = {"value": world * M * args.steps / (ms2 / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
+               "d2h_bytes_per_step": d2h,
+               "pipelining": "inputs of step k+1 copied on a second stream while step k computes"}
     st = int(status.item())
     if st != 0:
         raise RuntimeError(f"device status after timing: {orpo.orpo_status_string(st)}")
