@@ -17,6 +17,7 @@
 // flags the CTA as aborted and every role drains its own in-flight work and returns.
 #pragma once
 
+#include "../../include/orpo_head.h"
 #include "ptx.cuh"
 
 namespace orpo {
@@ -42,7 +43,6 @@ constexpr uint32_t SMEM_TOTAL = SMEM_CTL_OFF + SMEM_CTL_BYTES + 1024;  // + slac
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far above any legitimate wait
 
-constexpr int32_t kStatusTimeout = 1 << 8;  // ORPO_STATUS_TIMEOUT
 constexpr int RING = 4;                     // unit indices in flight between the roles (dynamic feed)
 
 struct SmemCtl {
@@ -138,7 +138,7 @@ __device__ __forceinline__ bool wait_phase(SmemCtl* ctl, uint64_t* bar, uint32_t
     if ((it & 63u) == 0) {
       if (ctl->abort_flag) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
-        atomicOr(status, kStatusTimeout);
+        atomicOr(status, ORPO_STATUS_TIMEOUT);
         ctl->abort_flag = 1;
         return false;
       }

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         gval = p.g[row];
         y = p.targets[row];
         if (y < 0 || y >= p.V) {
-          atomicOr(p.status, 1 << 4);
+          atomicOr(p.status, ORPO_STATUS_TARGET);
           y = -1;
         }
         lse2 = p.lse[row] * kLog2e;
@@ -220,13 +220,22 @@ struct GemmSched {
       default: return maps[5];
     }
   }
+  // class k by value, read through constant indices (no dynamically indexed copy of the table)
+  __device__ __forceinline__ GemmClass pick(int k) const {
+    GemmClass c;
+    if (k == 0)
+      c = cls[0];
+    else
+      c = cls[1];
+    return c;
+  }
   __device__ int n0() const { return cls[0].n_mt * cls[0].n_nt; }
   __device__ int num_units() const { return n0() + cls[1].n_mt * cls[1].n_nt; }
   __device__ int unit_len(int) const { return 1; }
   __device__ void decode(int u, int& k, int& mt, int& nt) const {
     k = u < n0() ? 0 : 1;
     const int v = k == 0 ? u : u - n0();
-    const GemmClass& c = cls[k];
+    const GemmClass c = pick(k);
     if (c.mt_major) {
       mt = v / c.n_nt;
       nt = v - mt * c.n_nt;
@@ -238,7 +247,7 @@ struct GemmSched {
   __device__ TileOps tile(int u, int) const {
     int k, mt, nt;
     decode(u, k, mt, nt);
-    const GemmClass& c = cls[k];
+    const GemmClass c = pick(k);
     TileOps t;
     t.a = Operand{map(c.a_map), c.a_mn, c.a_mn_base + mt * BM, c.a_k_base};
     t.b = Operand{map(c.b_map), c.b_mn, c.b_mn_base + nt * BN, c.b_k_base};
@@ -272,7 +281,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (u < 0) break;
       int k, mt, nt;
       sched.decode(u, k, mt, nt);
-      const GemmClass& c = sched.cls[k];
+      const GemmClass c = sched.pick(k);
       const CUtensorMap* out = sched.map(c.out_map);
       const int orow = c.out_row_base + mt * BM + 32 * q;
       const int ocol0 = c.out_col_base + nt * BN;
@@ -327,14 +336,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 namespace {
 template <int cap>
 cudaError_t launch_rec_kernel(const RecLaunch& L, cudaStream_t st) {
-  static int attr_set[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(rec_kernel<cap>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = 1;
-  }
+  static int smem_set[64] = {0};
+  if (cudaError_t e = opt_in_smem(rec_kernel<cap>, SMEM_TOTAL, smem_set)) return e;
   RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks, L.w_row0};
   RecArgs a{L.targets, L.mask, L.lse, L.g, L.M, L.V, L.softcap, L.status};
   prof_begin(K_REC, st);
@@ -352,14 +355,8 @@ cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st) {
 }
 
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
-  static int attr_set[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = 1;
-  }
+  static int smem_set[64] = {0};
+  if (cudaError_t e = opt_in_smem(gemm_kernel, SMEM_TOTAL, smem_set)) return e;
   GemmSched sched;
   for (int i = 0; i < 6; ++i) sched.maps[i] = nullptr;
   for (int k = 0; k < 2; ++k) {

@@ -200,12 +200,12 @@ __global__ void merge_kernel(const float* __restrict__ part_m, const float* __re
   const float l = (gm + log2f(S)) * kLn2;
   lse[t] = l;
   int32_t err = 0;
-  if (!isfinite(l)) err |= 1 << 7;
+  if (!isfinite(l)) err |= ORPO_STATUS_NONFINITE;
   float out = 0.f;
   if (mask[t] != 0) {
     const int y = targets[t];
     if (y < 0 || y >= V)
-      err |= 1 << 4;
+      err |= ORPO_STATUS_TARGET;
     else
       out = logp[t] - l;
   }
@@ -215,14 +215,8 @@ __global__ void merge_kernel(const float* __restrict__ part_m, const float* __re
 
 template <int cap>
 cudaError_t launch_fwd_kernel(const FwdLaunch& L, cudaStream_t st) {
-  static int attr_set[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<cap>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = 1;
-  }
+  static int smem_set[64] = {0};
+  if (cudaError_t e = opt_in_smem(fwd_kernel<cap>, SMEM_TOTAL, smem_set)) return e;
   FwdSched sched{nullptr, nullptr, L.n_mt, L.nsplit, L.n_vt, L.kblocks};
   FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M, L.Mpad, L.V, L.softcap, L.status, L.col0, L.split0};
   prof_begin(K_FWD, st);

@@ -7,6 +7,18 @@
 
 namespace orpo {
 
+// ---- kernels using more than 48 KiB of dynamic shared memory opt in once per device
+// (`done` is the caller's per-kernel table of devices already set)
+template <class Kernel>
+inline cudaError_t opt_in_smem(Kernel kernel, int bytes, int (&done)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= 64 || done[dev]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev] = 1;
+  return e;
+}
+
 // ---- launch timing (profile.cu); no-ops unless orpo_profile_start() was called
 enum KernelKind { K_FWD = 0, K_MERGE, K_LOSS, K_REC, K_GEMM, K_DEBUG, K_DEQUANT, K_NKINDS };
 void prof_begin(int kind, cudaStream_t st);

@@ -12,7 +12,8 @@
 // strictly inside a chunk is a whole sequence (ids are non-decreasing); the
 // first and last runs of each chunk are partial and are combined per sequence
 // by one warp in a fixed lane/butterfly order, so the result is bitwise
-// reproducible.  Per-pair arithmetic is fp64; outputs are fp32.
+// reproducible.  Sums and per-pair differences are fp64, the per-pair transcendentals fp32
+// (see log1mexp_d); outputs are fp32.
 //
 // The same kernel evaluates the sibling objectives that share the logp engine
 // ("Training — design" §8.3 SimPO; the xtrain post-training page's DPO with a
@@ -21,6 +22,7 @@
 // change, and whether a sequence is summarised by its mean or its sum.
 #include <math.h>
 
+#include "../../include/orpo_head.h"
 #include "internal.h"
 
 namespace orpo {
@@ -30,7 +32,8 @@ namespace {
 constexpr int T = 1024;
 constexpr int kKindOrpo = 0, kKindSimpo = 1, kKindDpo = 2, kKindIpo = 3, kKindHinge = 4, kKindOrpoFull = 5;
 constexpr uint8_t kPromptRow = 2;  // mask value: prompt row, supervised only by the full-scope NLL
-constexpr int32_t kSeqErr = 1 << 5, kEmptyErr = 1 << 6, kNonfiniteErr = 1 << 7;
+constexpr int32_t kSeqErr = ORPO_STATUS_SEQID, kEmptyErr = ORPO_STATUS_EMPTY_SEQ,
+                  kNonfiniteErr = ORPO_STATUS_NONFINITE;
 
 struct LossSmem {
   int head_sid[T], tail_sid[T], first_sid[T], last_sid[T];
@@ -41,19 +44,30 @@ struct LossSmem {
   double red[5][T / 32];
   int err;
 };
-// followed by: double seq_sum[S]; int seq_cnt[S]; double G[S]; double seq_fsum[S]; int seq_fcnt[S]
+// followed by: double seq_sum[S]; int seq_cnt[S]; double G[S]; double seq_fsum[S]; int seq_fcnt[S];
+//               float coef[S]; float coef_full[S]
 
+// Per-pair transcendentals run in fp32 (the library's accurate logf / expm1f / log1pf / expf, a few
+// ulp): double-precision transcendentals are very slow on this GPU and sit on a serial per-pair
+// chain.  Their arguments (means, sums, log-ratio differences) are formed in fp64 first, so no
+// cancellation happens in fp32; values return to fp64 for the reductions.
 __device__ __forceinline__ double log1mexp_d(double x) {
   // log(1 - e^x), x <= 0; two branches at -ln 2 (Maechler 2012)
-  return x > -0.6931471805599453 ? log(-expm1(x)) : log1p(-exp(x));
+  const float xf = (float)x;
+  return (double)(x > -0.6931471805599453 ? logf(-expm1f(xf)) : log1pf(-expf(xf)));
 }
 
-__device__ __forceinline__ double softplus_d(double x) { return fmax(x, 0.0) + log1p(exp(-fabs(x))); }
+__device__ __forceinline__ double softplus_d(double x) {
+  return fmax(x, 0.0) + (double)log1pf(expf(-(float)fabs(x)));
+}
 
 __device__ __forceinline__ double sigmoid_d(double x) {
-  const double e = exp(-fabs(x));
-  return x >= 0 ? 1.0 / (1.0 + e) : e / (1.0 + e);
+  const float e = expf(-(float)fabs(x));
+  return (double)(x >= 0 ? 1.f / (1.f + e) : e / (1.f + e));
 }
+
+// 1 / (1 - e^l) = -1 / expm1(l), l <= 0
+__device__ __forceinline__ double inv_one_minus_exp(double l) { return (double)(-1.f / expm1f((float)l)); }
 
 __global__ void __launch_bounds__(T, 1)
     loss_kernel(int kind, const float* __restrict__ logp, const int32_t* __restrict__ seq_id,
@@ -220,7 +234,7 @@ __global__ void __launch_bounds__(T, 1)
       const double x = (lw - lr) - (log1mexp_d(lw) - log1mexp_d(lr));
       term = softplus_d(-x);
       const double sg = sigmoid_d(-x);
-      const double inv_w = -1.0 / expm1(lw), inv_r = -1.0 / expm1(lr);  // 1 / (1 - e^l)
+      const double inv_w = inv_one_minus_exp(lw), inv_r = inv_one_minus_exp(lr);
       // response scope folds the NLL gradient (-1/P on l_w) into G_w; full scope spreads
       // -1/(P N_w) over the chosen prompt + response rows in phase 5
       if (full_scope) nll_p = -seq_fsum[2 * p] / (double)seq_fcnt[2 * p];
@@ -290,17 +304,25 @@ __global__ void __launch_bounds__(T, 1)
     if (lane == 0 && sm.err) atomicOr(status, sm.err);
   }
 
-  // ---- phase 5: per-token gradient
+  // ---- phase 5: per-sequence coefficients (fp64 once per sequence), then the per-token gradient
+  // as a plain fp32 lookup: g_t = coef[s] on response rows, plus coef_full[s] on every supervised
+  // row of a chosen sequence under the full-scope NLL
+  float* coef = reinterpret_cast<float*>(seq_fcnt + S);
+  float* coef_full = coef + S;
+  for (int s2 = tid; s2 < S; s2 += T) {
+    const int n = seq_cnt[s2];
+    coef[s2] = n > 0 ? (float)(mean_kind ? G[s2] / (double)n : G[s2]) : 0.f;
+    coef_full[s2] = (full_scope && (s2 & 1) == 0 && seq_fcnt[s2] > 0)
+                        ? (float)(-1.0 / ((double)P * seq_fcnt[s2]))
+                        : 0.f;
+  }
+  __syncthreads();
   for (int t = tid; t < M; t += T) {
     const int sid = seq_id[t];
     const uint8_t mk = mask[t];
-    double gv = 0.0;
-    if (sid >= 0 && sid < S && mk != 0) {
-      const int n = seq_cnt[sid];
-      if (mk != kPromptRow && n > 0) gv = mean_kind ? G[sid] / (double)n : G[sid];
-      if (full_scope && (sid & 1) == 0 && seq_fcnt[sid] > 0) gv += -1.0 / ((double)P * seq_fcnt[sid]);
-    }
-    g[t] = (float)gv;
+    float gv = 0.f;
+    if (sid >= 0 && sid < S && mk != 0) gv = (mk != kPromptRow ? coef[sid] : 0.f) + coef_full[sid];
+    g[t] = gv;
   }
 }
 
@@ -308,15 +330,22 @@ __global__ void __launch_bounds__(T, 1)
 
 size_t loss_smem_bytes(int P) {
   const size_t S = 2 * (size_t)P;
-  return sizeof(LossSmem) + S * 8 + ((S * 4 + 7) & ~size_t(7)) + S * 8 + S * 8 + S * 4;
+  return sizeof(LossSmem) + S * 8 + ((S * 4 + 7) & ~size_t(7)) + S * 8 + S * 8 + S * 4 + 2 * S * 4;
 }
 
 cudaError_t launch_loss(int kind, const float* logp, const int32_t* seq_id, const uint8_t* mask, int M, int P,
                         float beta, float gamma, const float* ref, float* out, float* ell, float* g, int32_t* status,
                         cudaStream_t st) {
   const size_t smem = loss_smem_bytes(P);
-  cudaError_t e = cudaFuncSetAttribute(loss_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  // raise the kernel's dynamic shared-memory limit only when a larger size than before is needed
+  static int limit[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || (int)smem > limit[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(loss_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) limit[dev] = (int)smem;
+  }
   prof_begin(K_LOSS, st);
   loss_kernel<<<1, T, smem, st>>>(kind, logp, seq_id, mask, M, P, beta, gamma, ref, out, ell, g, status);
   prof_end(K_LOSS, st);
