@@ -137,6 +137,21 @@ int choose_nsplit(int64_t n_mt, int64_t n_vt, int sms) {
   return best;
 }
 
+// Forward launch shape.  Pair mode (2-CTA clusters sharing each W tile) when at least two row
+// tiles exist and padding an odd count to even wastes little; then the units along M are row-tile
+// pairs and the slots are co-resident clusters.
+struct FwdShape {
+  int pair;
+  int64_t units_m;  // row tiles, or row-tile pairs in pair mode
+  int slots;        // CTAs, or clusters in pair mode
+};
+
+FwdShape forward_shape(int64_t n_mt, int sms) {
+  const int clusters = (n_mt >= 2 && (n_mt % 2 == 0 || n_mt >= 16)) ? forward_pair_clusters() : 0;
+  if (clusters > 0) return FwdShape{1, (n_mt + 1) / 2, clusters};
+  return FwdShape{0, n_mt, sms};
+}
+
 }  // namespace
 
 bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
@@ -237,6 +252,9 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   const int64_t nblocks = cdiv(V, vb);
   const int per_block = std::max<int>(1, nsplit_max / (int)nblocks);
   void* Wb = q ? wblock_ptr(workspace, M, V) : nullptr;
+  const FwdShape fs = forward_shape(n_mt, sms);
+  L.pair = fs.pair;
+  const uint32_t w_box = fs.pair ? kBN / 2 : kBN;
   int split0 = 0;
   for (int64_t v0 = 0; v0 < V; v0 += vb) {
     const int64_t vc = std::min(vb, V - v0);
@@ -244,15 +262,15 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
     if (q) {
       if (launch_dequant(q->wq, q->scales, q->biases, q->bits, q->group, v0, vc, d, Wb, st) != cudaSuccess)
         return ORPO_ERR_CUDA;
-      if (!encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Wb, d, vc, d * 2, 64, kBN)) return ORPO_ERR_CUDA;
-    } else if (!encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, kBN)) {
+      if (!encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Wb, d, vc, d * 2, 64, w_box)) return ORPO_ERR_CUDA;
+    } else if (!encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, w_box)) {
       return ORPO_ERR_CUDA;
     }
     L.n_vt = (int)n_vt;
-    L.nsplit = std::min<int>(choose_nsplit(n_mt, n_vt, sms), per_block);
+    L.nsplit = std::min<int>(choose_nsplit(fs.units_m, n_vt, fs.slots), per_block);
     L.col0 = (int)v0;
     L.split0 = split0;
-    L.grid = (int)std::min<int64_t>(n_mt * L.nsplit, sms);
+    L.grid = (int)std::min<int64_t>(fs.units_m * L.nsplit, fs.slots) * (fs.pair ? 2 : 1);
     if (launch_forward_logits(L, st) != cudaSuccess) return ORPO_ERR_CUDA;
     split0 += L.nsplit;
   }

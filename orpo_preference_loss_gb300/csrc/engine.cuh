@@ -66,17 +66,23 @@ struct SmemCtl {
 struct Feed {
   int* counter;
   int nu;
+  int first = -1;  // static feed: first unit and stride (default: blockIdx.x, gridDim.x)
+  int stride = 0;
 };
+
+__device__ __forceinline__ int static_unit(const Feed& f, uint32_t i) {
+  const long long first = f.first >= 0 ? f.first : blockIdx.x;
+  const long long stride = f.stride > 0 ? f.stride : gridDim.x;
+  const long long u = first + (long long)i * stride;
+  return u < f.nu ? (int)u : -1;
+}
 
 __device__ __forceinline__ bool wait_phase(SmemCtl* ctl, uint64_t* bar, uint32_t parity, int32_t* status,
                                            uint64_t limit_ns = kWaitLimitNs);
 
 // Producer side: returns the next unit, -1 when done, -2 on abort.
 __device__ __forceinline__ int feed_produce(const Feed& f, SmemCtl* ctl, uint32_t i, int32_t* status) {
-  if (f.counter == nullptr) {
-    const long long u = (long long)blockIdx.x + (long long)i * gridDim.x;
-    return u < f.nu ? (int)u : -1;
-  }
+  if (f.counter == nullptr) return static_unit(f, i);
   const uint32_t r = i % RING, ph = (i / RING) & 1u;
   if (!wait_phase(ctl, &ctl->unit_empty[r], ph ^ 1u, status)) return -2;
   int u = atomicAdd(f.counter, 1);
@@ -89,10 +95,7 @@ __device__ __forceinline__ int feed_produce(const Feed& f, SmemCtl* ctl, uint32_
 // Consumer side (the MMA thread, or a whole epilogue warp): same sequence as the producer's.
 __device__ __forceinline__ int feed_consume(const Feed& f, SmemCtl* ctl, uint32_t i, int32_t* status,
                                             bool whole_warp) {
-  if (f.counter == nullptr) {
-    const long long u = (long long)blockIdx.x + (long long)i * gridDim.x;
-    return u < f.nu ? (int)u : -1;
-  }
+  if (f.counter == nullptr) return static_unit(f, i);
   const uint32_t r = i % RING, ph = (i / RING) & 1u;
   if (!wait_phase(ctl, &ctl->unit_full[r], ph, status)) return -2;
   const int u = ctl->unit_ring[r];
@@ -166,6 +169,12 @@ __device__ __forceinline__ void load_operand(const Operand& op, uint64_t* bar, u
   }
 }
 
+// Paired mode: this CTA fetches its half of the B tile (rows [rank * BN/2, (rank + 1) * BN/2) of a
+// K-major tile, through a map whose box is {64, BN/2}) and multicasts it to both CTAs of the cluster.
+__device__ __forceinline__ void load_b_half(const Operand& op, uint64_t* bar, uint8_t* b_dst, int kb, uint32_t rank) {
+  tma_load_2d_mc(op.map, bar, b_dst + rank * (B_BYTES / 2), op.k0 + kb * BK, op.mn0 + (int)rank * (BN / 2), 0x3);
+}
+
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, int kk) {
   // K-major: advance 16 elements (32 B) inside the swizzle row; MN-major: advance 16 k-rows (2 KiB)
   return mn_major ? smem_desc_sw128(base + kk * (UMMA_K * 128), BK * 128, 1024)
@@ -173,8 +182,9 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, in
 }
 
 // ---------------------------------------------------------------- producer (one thread)
-template <class Sched>
+template <bool kPair, class Sched>
 __device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* smem, SmemCtl* ctl, int32_t* status) {
+  const uint32_t rank = kPair ? cluster_ctarank() : 0;
   uint32_t it = 0;
   bool ok = true;
   for (uint32_t i = 0; ok; ++i) {
@@ -194,9 +204,12 @@ __device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* sme
         }
         uint8_t* a_dst = smem + s * STAGE_BYTES;
         uint8_t* b_dst = a_dst + A_BYTES;
-        mbar_arrive_expect_tx(&ctl->full[s], STAGE_BYTES);
+        mbar_arrive_expect_tx(&ctl->full[s], STAGE_BYTES);  // paired: half of B comes from the peer
         load_operand(t.a, &ctl->full[s], a_dst, BM, kb);
-        load_operand(t.b, &ctl->full[s], b_dst, BN, kb);
+        if constexpr (kPair)
+          load_b_half(t.b, &ctl->full[s], b_dst, kb, rank);
+        else
+          load_operand(t.b, &ctl->full[s], b_dst, BN, kb);
       }
     }
   }
@@ -208,7 +221,7 @@ __device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* sme
 }
 
 // ---------------------------------------------------------------- MMA issuer (one thread)
-template <class Sched>
+template <bool kPair, class Sched>
 __device__ void mma_role(const Sched& sched, const Feed& feed, uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base,
                          int32_t* status) {
   uint32_t it = 0, tcount = 0;
@@ -242,7 +255,12 @@ __device__ void mma_role(const Sched& sched, const Feed& feed, uint8_t* smem, Sm
           umma_bf16(d_tmem, operand_desc(a_base, t.a.mn_major != 0, kk), operand_desc(b_base, t.b.mn_major != 0, kk), idesc,
                     (kb | kk) != 0 ? 1u : 0u);
         }
-        umma_commit(&ctl->empty[s]);  // frees the stage once these MMAs have read it
+        // frees the stage once these MMAs have read it (paired: in both CTAs, whose producers
+        // write halves of B into each other's stage)
+        if constexpr (kPair)
+          umma_commit_mc(&ctl->empty[s], 0x3);
+        else
+          umma_commit(&ctl->empty[s]);
       }
       if (!ok) break;
       umma_commit(&ctl->acc_full[buf]);  // accumulator ready for the epilogue
@@ -294,7 +312,7 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t box, int lane, const uin
 
 // Runs the three roles; `epilogue(smem, ctl, tmem_base, warp, lane)` is the kernel's epilogue loop,
 // which walks the units with feed_consume(feed, ctl, i, status, true).
-template <class Sched, class EpiFn>
+template <bool kPair = false, class Sched, class EpiFn>
 __device__ __forceinline__ void run_cta(const Sched& sched, const Feed& feed, int32_t* status, EpiFn&& epilogue) {
   uint8_t* smem = smem_base_aligned();
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + SMEM_CTL_OFF);
@@ -302,7 +320,7 @@ __device__ __forceinline__ void run_cta(const Sched& sched, const Feed& feed, in
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], 1);
+      mbar_init(&ctl->empty[s], kPair ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->acc_full[b], 1);
@@ -322,19 +340,21 @@ __device__ __forceinline__ void run_cta(const Sched& sched, const Feed& feed, in
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer_role(sched, feed, smem, ctl, status);
+    if (lane == 0) producer_role<kPair>(sched, feed, smem, ctl, status);
   } else if (warp == 1) {
-    if (lane == 0) mma_role(sched, feed, smem, ctl, tmem_base, status);
+    if (lane == 0) mma_role<kPair>(sched, feed, smem, ctl, tmem_base, status);
   } else {
     epilogue(smem, ctl, tmem_base, warp, lane);
   }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();  // no CTA leaves while its peer may still write into it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);

@@ -21,18 +21,28 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Pair mode: the CTAs of a 2-CTA cluster take row tiles 2p and 2p + 1 of the same split, walk the
+// same vocabulary tiles in lockstep, and each fetches half of every W tile for both (TMA multicast),
+// so W crosses from L2 to the SMs once per pair of row tiles instead of once per row tile.
 struct FwdSched {
   const CUtensorMap* mh;
   const CUtensorMap* mw;
-  int n_mt, nsplit, n_vt, kblocks;
-  __device__ int num_units() const { return n_mt * nsplit; }
+  int n_mt, nsplit, n_vt, kblocks;  // pair mode: n_mt is even
+  int pair, rank;                   // pair mode flag; this CTA's rank in its cluster (0 otherwise)
+  __device__ int n_mu() const { return pair ? n_mt >> 1 : n_mt; }
+  __device__ int num_units() const { return n_mu() * nsplit; }
+  __device__ int split_of(int u) const { return u / n_mu(); }
+  __device__ int mt_of(int u) const {
+    const int m = u - split_of(u) * n_mu();
+    return pair ? 2 * m + rank : m;
+  }
   __device__ int vt_begin(int s) const { return (int)(((long long)s * n_vt) / nsplit); }
   __device__ int unit_len(int u) const {
-    const int s = u / n_mt;
+    const int s = split_of(u);
     return vt_begin(s + 1) - vt_begin(s);
   }
   __device__ TileOps tile(int u, int j) const {
-    const int s = u / n_mt, mt = u - s * n_mt;
+    const int s = split_of(u), mt = mt_of(u);
     const int vt = vt_begin(s) + j;
     TileOps t;
     t.a = Operand{mh, 0, mt * BM, 0};
@@ -136,18 +146,22 @@ __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, in
   st.m = mnew;
 }
 
-template <int cap>
+template <int cap, bool kPair>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mw, FwdSched sched,
                FwdArgs p) {
   sched.mh = &mh;
   sched.mw = &mw;
+  sched.pair = kPair ? 1 : 0;
+  sched.rank = kPair ? (int)cluster_ctarank() : 0;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&mh);
     tma_prefetch_desc(&mw);
   }
-  const Feed feed{nullptr, sched.num_units()};
-  run_cta(sched, feed, p.status, [&](uint8_t*, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
+  // pair mode: cluster c takes pair units c, c + C, ... (C clusters; 1-D grid, rank = blockIdx.x % 2)
+  const Feed feed = kPair ? Feed{nullptr, sched.num_units(), (int)(blockIdx.x >> 1), (int)(gridDim.x >> 1)}
+                          : Feed{nullptr, sched.num_units()};
+  run_cta<kPair>(sched, feed, p.status, [&](uint8_t*, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
     const int q = warp & 3;
     const float inv_c = cap != kCapOff ? 1.f / p.softcap : 0.f;
     const float cl2 = p.softcap * kLog2e;
@@ -155,7 +169,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (uint32_t i = 0;; ++i) {
       const int u = feed_consume(feed, ctl, i, p.status, true);
       if (u < 0) break;
-      const int s = u / sched.n_mt, mt = u - s * sched.n_mt;
+      const int s = sched.split_of(u), mt = sched.mt_of(u);
       const int row = mt * BM + 32 * q + lane;
       int y = -1;
       if (row < p.M && p.mask[row] != 0) y = p.targets[row];
@@ -180,8 +194,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         epi_release(ctl, tcount);
       }
-      p.part_m[(size_t)(p.split0 + s) * p.Mpad + row] = st.m;
-      p.part_s[(size_t)(p.split0 + s) * p.Mpad + row] = st.s;
+      if (row < p.Mpad) {  // pair mode pads an odd tile count with one empty tile
+        p.part_m[(size_t)(p.split0 + s) * p.Mpad + row] = st.m;
+        p.part_s[(size_t)(p.split0 + s) * p.Mpad + row] = st.s;
+      }
     }
   });
 }
@@ -213,25 +229,74 @@ __global__ void merge_kernel(const float* __restrict__ part_m, const float* __re
   if (err) atomicOr(status, err);
 }
 
-template <int cap>
+template <int cap, bool kPair>
 cudaError_t launch_fwd_kernel(const FwdLaunch& L, cudaStream_t st) {
   static int smem_set[64] = {0};
-  if (cudaError_t e = opt_in_smem(fwd_kernel<cap>, SMEM_TOTAL, smem_set)) return e;
-  FwdSched sched{nullptr, nullptr, L.n_mt, L.nsplit, L.n_vt, L.kblocks};
+  if (cudaError_t e = opt_in_smem(fwd_kernel<cap, kPair>, SMEM_TOTAL, smem_set)) return e;
+  const int n_mt = kPair ? (L.n_mt + 1) & ~1 : L.n_mt;
+  FwdSched sched{nullptr, nullptr, n_mt, L.nsplit, L.n_vt, L.kblocks, 0, 0};
   FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M, L.Mpad, L.V, L.softcap, L.status, L.col0, L.split0};
+  cudaError_t e = cudaSuccess;
   prof_begin(K_FWD, st);
-  fwd_kernel<cap><<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, sched, a);
+  if constexpr (kPair) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)L.grid);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_TOTAL;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fwd_kernel<cap, true>, L.mh, L.mw, sched, a);
+  } else {
+    fwd_kernel<cap, false><<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, sched, a);
+  }
   prof_end(K_FWD, st);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <bool kPair>
+cudaError_t launch_fwd_cap(const FwdLaunch& L, cudaStream_t st) {
+  const int cap = L.softcap > 0.f ? (L.softcap <= kCapExpMax ? kCapExp : kCapHybrid) : kCapOff;
+  return cap == kCapExp      ? launch_fwd_kernel<kCapExp, kPair>(L, st)
+         : cap == kCapHybrid ? launch_fwd_kernel<kCapHybrid, kPair>(L, st)
+                             : launch_fwd_kernel<kCapOff, kPair>(L, st);
 }
 
 }  // namespace
 
+int forward_pair_clusters() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] != 0) return cached[dev] > 0 ? cached[dev] : 0;
+  static int smem_set[64] = {0};
+  int n = 0;
+  if (opt_in_smem(fwd_kernel<kCapExp, true>, SMEM_TOTAL, smem_set) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_TOTAL;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, fwd_kernel<kCapExp, true>, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  cached[dev] = n > 0 ? n : -1;
+  return n > 0 ? n : 0;
+}
+
 cudaError_t launch_forward_logits(const FwdLaunch& L, cudaStream_t st) {
-  const int cap = L.softcap > 0.f ? (L.softcap <= kCapExpMax ? kCapExp : kCapHybrid) : kCapOff;
-  return cap == kCapExp      ? launch_fwd_kernel<kCapExp>(L, st)
-         : cap == kCapHybrid ? launch_fwd_kernel<kCapHybrid>(L, st)
-                             : launch_fwd_kernel<kCapOff>(L, st);
+  return L.pair ? launch_fwd_cap<true>(L, st) : launch_fwd_cap<false>(L, st);
 }
 
 cudaError_t launch_forward_merge(const FwdLaunch& L, int nsplit_total, cudaStream_t st) {

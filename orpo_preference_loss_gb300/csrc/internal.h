@@ -47,7 +47,9 @@ struct FwdLaunch {
   int grid;
   int col0 = 0;    // vocabulary column of row 0 of mw
   int split0 = 0;  // first split index this launch writes
+  int pair = 0;    // 1: 2-CTA clusters share W tiles (mw box {64,128}; grid = 2 x clusters; n_mt padded to even)
 };
+int forward_pair_clusters();  // co-resident 2-CTA clusters of the forward kernel (0: pair mode unavailable)
 cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st);  // logits kernel + merge of L.nsplit splits
 cudaError_t launch_forward_logits(const FwdLaunch& L, cudaStream_t st);
 cudaError_t launch_forward_merge(const FwdLaunch& L, int nsplit_total, cudaStream_t st);
