@@ -14,6 +14,10 @@ from .orpo_oracle import (  # noqa: F401
     head_forward,
     orpo_loss,
     head_backward,
+    head_block_max,
+    TILE_ROWS,
+    TILE_COLS,
+    GROUP_ROWS,
     full_chain,
     pref_loss,
     PREF_KINDS,

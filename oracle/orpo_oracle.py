@@ -31,7 +31,11 @@ segmented backward)" page, and the "Steel flash-CCE — handoff" page):
 * ``head_backward`` — implementation spec, backward bullet: recompute the
   logits, ``dZ = g * (onehot_y - softmax(z~)) * sech^2(z / c)``, then
   ``dh = dZ W`` and (the head-weight gradient that the pages leave to the
-  head-LoRA follow-on) ``dW = dZ^T h``.
+  head-LoRA follow-on) ``dW = dZ^T h``.  Optionally with the coefficient
+  filter of the backward skips ("Steel flash-CCE — handoff" §E; "Training —
+  design" §5.1): tiles of the coefficient that lie wholly below eps are dropped.
+* ``head_block_max`` — the forward's per-(row group, vocabulary tile) maxima of
+  the softcapped logits that the block skip reads (handoff §E, blockMax).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, library routines, invariants and central finite differences).
@@ -266,13 +270,74 @@ def orpo_loss(logp: np.ndarray, seq_id: np.ndarray, mask: np.ndarray, n_pairs: i
 # head backward: dh and dW
 # --------------------------------------------------------------------------
 
+TILE_ROWS, TILE_COLS = 128, 256   # tile of the backward skips (rows x vocabulary columns)
+GROUP_ROWS = 32                    # row group of the forward's block maxima
+
+
+def _tile_keep(coef: np.ndarray, active: np.ndarray, eps: float, tile=(TILE_ROWS, TILE_COLS)) -> np.ndarray:
+    """Element mask of the tiles that the coefficient filter keeps.
+
+    "Steel flash-CCE — handoff" §E (coefficient filter) and "Training — design"
+    §5.1 (the Apple-CCE backward skips, default eps 1e-5): a block of the
+    coefficient whose entries all lie below eps is skipped.  The block here is a
+    tile of ``tile`` rows x columns aligned to row 0 and vocabulary column 0 of
+    the whole [M, V] coefficient, and the coefficient is the part of dZ that
+    does not depend on the batch scale, (onehot - p) sech^2, taken over the rows
+    whose cotangent g is nonzero (the other rows' dZ is identically 0).  A tile
+    is kept when one such entry has magnitude >= eps.  ``coef`` holds a row
+    chunk that starts on a tile boundary.
+    """
+    tr, tc = tile
+    R, V = coef.shape
+    a = np.where(active[:, None], np.abs(coef), 0.0)
+    nr, nc = -(-R // tr), -(-V // tc)
+    padded = np.zeros((nr * tr, nc * tc))
+    padded[:R, :V] = a
+    keep = padded.reshape(nr, tr, nc, tc).max(axis=(1, 3)) >= eps
+    return np.repeat(np.repeat(keep, tr, axis=0), tc, axis=1)[:R, :V]
+
+
+def head_block_max(h: np.ndarray, W: np.ndarray, mask: np.ndarray, softcap: float = 0.0,
+                   group=(GROUP_ROWS, TILE_COLS)) -> np.ndarray:
+    """Block maxima of the softcapped logits, in base-2 units (z~ log2 e).
+
+    "Steel flash-CCE — handoff" §E (blockMax vocabulary-block skip: the
+    backward skips cold (token block, vocabulary block) programs using the
+    forward's blockMax).  Entry [q, j] is the largest z~[t, v] log2(e) over the
+    rows t of row group q (``group[0]`` rows from row 0) with mask != 0 and the
+    columns v of vocabulary tile j (``group[1]`` columns); -inf where the group
+    has no such row.  Shape [ceil(M / group[0]), ceil(V / group[1])].
+    """
+    h = np.asarray(h, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    M, V = h.shape[0], W.shape[0]
+    gr, gc = group
+    nq, nj = -(-M // gr), -(-V // gc)
+    mask = np.asarray(mask).astype(bool)
+    out = np.full((nq, nj), -np.inf)
+    step = max(gr, _row_chunk(V) // gr * gr)
+    for r0 in range(0, M, step):
+        r1 = min(M, r0 + step)
+        z = softcap_value(h[r0:r1] @ W.T, softcap) / LN2
+        z[~mask[r0:r1]] = -np.inf
+        R = r1 - r0
+        padded = np.full((-(-R // gr) * gr, nj * gc), -np.inf)
+        padded[:R, :V] = z
+        out[r0 // gr:r0 // gr + padded.shape[0] // gr] = padded.reshape(-1, gr, nj, gc).max(axis=(1, 3))
+    return out
+
+
 def head_backward(h: np.ndarray, W: np.ndarray, targets: np.ndarray, mask: np.ndarray,
-                  lse: np.ndarray, g: np.ndarray, softcap: float = 0.0):
+                  lse: np.ndarray, g: np.ndarray, softcap: float = 0.0, filter_eps: float = 0.0,
+                  tile=(TILE_ROWS, TILE_COLS)):
     """dh = dZ W and dW = dZ^T h with dZ = g (onehot_y - softmax(z~)) sech^2(z/c).
 
     softmax is rebuilt from the given lse: p = exp(z~ - lse).  Rows with
     mask = 0 carry no gradient (their g is treated as 0 and their target is not
-    read).  Returns (dh [M, d], dW [V, d]) in float64.
+    read).  With ``filter_eps`` > 0 the coefficient filter of the backward
+    skips applies: every ``tile`` of dZ whose coefficient entries all lie below
+    filter_eps is dropped (see ``_tile_keep``).  Returns (dh [M, d], dW [V, d])
+    in float64.
     """
     h = np.asarray(h, dtype=np.float64)
     W = np.asarray(W, dtype=np.float64)
@@ -285,6 +350,8 @@ def head_backward(h: np.ndarray, W: np.ndarray, targets: np.ndarray, mask: np.nd
     dh = np.zeros((M, d))
     dW = np.zeros((V, d))
     step = _row_chunk(V)
+    if filter_eps > 0:
+        step = max(tile[0], step // tile[0] * tile[0])  # chunks start on tile boundaries
     for r0 in range(0, M, step):
         r1 = min(M, r0 + step)
         gr = g[r0:r1]
@@ -297,7 +364,10 @@ def head_backward(h: np.ndarray, W: np.ndarray, targets: np.ndarray, mask: np.nd
         rows = np.arange(r1 - r0)
         m = mask[r0:r1]
         onehot[rows[m], targets[r0:r1][m]] = 1.0
-        dZ = gr[:, None] * (onehot - p) * softcap_slope(z, softcap)
+        coef = (onehot - p) * softcap_slope(z, softcap)
+        if filter_eps > 0:
+            coef = np.where(_tile_keep(coef, gr != 0.0, filter_eps, tile), coef, 0.0)
+        dZ = gr[:, None] * coef
         dh[r0:r1] = dZ @ W
         dW += dZ.T @ h[r0:r1]
     return dh, dW
