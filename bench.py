@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="e4b", choices=["tiny", "small", "e4b", "largev", "ragged"])
+    ap.add_argument("--workload", default="e4b", choices=["tiny", "small", "e4b", "largev", "ragged", "e4b_sharp"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--quant", type=int, default=0, choices=[0, 4, 8],
                     help="run the quantised head: W as 4/8-bit affine groups of 64 (0 = bf16 head)")
     ap.add_argument("--frozen", action="store_true", help="frozen head: skip dW")
+    ap.add_argument("--skip-eps", type=float, default=0.0,
+                    help="backward skips (coefficient filter + block skip) at this eps; 0 = exact backward")
     ap.add_argument("--M", type=int, default=None, help="shrink the workload's rows (profiling cases)")
     ap.add_argument("--V", type=int, default=None, help="shrink the vocabulary (profiling cases)")
     ap.add_argument("--d", type=int, default=None, help="change the hidden size (profiling cases)")
@@ -263,6 +265,10 @@ def ours(args, w, rank, world, local):
     dh = torch.empty((M, d), dtype=torch.float32, device=dev)
     dW = None if args.frozen else torch.empty((V, d), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    skip = args.skip_eps > 0
+    if skip and args.quant:
+        raise SystemExit("--skip-eps runs on the bf16 head")
+    bmax = torch.empty(orpo.block_max_shape(M, V), dtype=torch.float32, device=dev) if skip else None
     # cached reference sums for the DPO-family objectives: seeded synthetic values per sequence
     ref = torch.from_numpy((-6.0 * np.bincount(np.maximum(w.seq_id, 0), minlength=2 * P)[:2 * P]
                             + np.random.default_rng(17).standard_normal(2 * P)).astype(np.float32)).to(dev)
@@ -285,6 +291,8 @@ def ours(args, w, rank, world, local):
         hv, wv = views(inp)
         if args.quant:
             orpo.orpo_head_fwd_q(hv, *wv, inp["targets"], inp["mask"], w.softcap, logp, lse, ws, status)
+        elif skip:
+            orpo.orpo_head_fwd_bmax(hv, wv, inp["targets"], inp["mask"], w.softcap, logp, lse, bmax, ws, status)
         else:
             orpo.orpo_head_fwd(hv, wv, inp["targets"], inp["mask"], w.softcap, logp, lse, ws, status)
         if args.loss == "orpo":
@@ -293,6 +301,9 @@ def ours(args, w, rank, world, local):
             orpo.orpo_pref_loss(args.loss, logp, inp["seq_id"], inp["mask"], P, beta, 0.5, ref, out, ell, g, status)
         if args.quant:
             orpo.orpo_head_bwd_q(hv, *wv, inp["targets"], inp["mask"], lse, g, w.softcap, dh, dW, False, ws, status)
+        elif skip:
+            orpo.orpo_head_bwd_skip(hv, wv, inp["targets"], inp["mask"], lse, g, bmax, args.skip_eps, w.softcap, dh,
+                                    dW, False, ws, status)
         else:
             orpo.orpo_head_bwd(hv, wv, inp["targets"], inp["mask"], lse, g, w.softcap, dh, dW, False, ws, status)
 
@@ -390,6 +401,8 @@ def ours(args, w, rank, world, local):
     kflops = {"fwd_logits": 2.0 * M * V * d * args.steps,
               "bwd_recompute": 2.0 * M * V * d * args.steps,
               "bwd_grad_gemm": (2.0 if args.frozen else 4.0) * M * V * d * args.steps}
+    if skip:  # the skipped backward's work depends on the data: only the forward keeps a dense count
+        del kflops["bwd_recompute"], kflops["bwd_grad_gemm"]
     kernels = {}
     for name, (kms, cnt) in prof.items():
         if cnt == 0:
@@ -411,6 +424,8 @@ def ours(args, w, rank, world, local):
             "config": dict(workload_config(w), objective=args.loss,
                            head=f"{args.quant}-bit affine groups of 64" if args.quant else "bf16",
                            dW="skipped (frozen head)" if args.frozen else "computed",
+                           backward=(f"skips at eps {args.skip_eps:g} (coefficient filter + block skip); "
+                                     "tflops counts the dense 6MVd" if skip else "exact"),
                            parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
             "tflops": tflops, "frac_of_peak": tflops / sustained, "frac_of_burst_peak": tflops / burst,
             "peak_extra_gb": peak_extra / 1e9, "e2e": e2e, "gpu_launches": sum(v["launches"] for v in

@@ -220,6 +220,46 @@ int orpo_head_bwd_q(const void* h_bf16, const uint8_t* wq, const void* scales_bf
                     int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* status,
                     void* stream);
 
+/*
+ * Backward skips ("Steel flash-CCE — handoff" §E, coefficient filter and
+ * blockMax vocabulary-block skip; "Training — design" §5.1, the Apple-CCE skips
+ * with eps 1e-5 by default).  An approximation that drops the parts of the
+ * logit gradient that lie wholly below eps.  Its unit is one tile of 128 rows x
+ * 256 vocabulary columns of dZ, aligned to row 0 and column 0.
+ *
+ * Coefficient filter: a tile is dropped when no row t with g[t] != 0 has an
+ * entry with |(onehot - p) sech^2| >= eps in it; dropped tiles contribute
+ * nothing to dh or dW, kept tiles contribute exactly what orpo_head_bwd would.
+ * Block skip: the forward's block maxima (orpo_head_fwd_bmax) bound p from
+ * above; a tile that holds no target of a row with g != 0 and whose bound lies
+ * below eps is not recomputed at all.  The filter would drop every such tile,
+ * so the block skip changes no result bit; it only saves the recompute.
+ *
+ * orpo_head_block_max_elems(M, V) = ceil(M / 32) * ceil(V / 256): floats of the
+ *   block-max array.
+ * orpo_head_fwd_bmax: orpo_head_fwd, and it also writes block_max (fp32,
+ *   [ceil(M/32)][ceil(V/256)], row-major, 4-byte aligned; caller-owned): entry
+ *   [q][j] = max of z~[t, v] * log2(e) over the rows t of group q (rows 32q ..
+ *   32q+31) with mask != 0 and the columns v of tile j (256j .. 256j+255);
+ *   -inf when the group has no such row.
+ * orpo_head_bwd_skip: orpo_head_bwd with the coefficient filter at threshold
+ *   eps (0 <= eps, finite; eps = 0 is exactly orpo_head_bwd).  block_max, when
+ *   not NULL, must be what orpo_head_fwd_bmax wrote for the same h, W, mask and
+ *   softcap; it enables the block skip.  NULL runs the filter alone.
+ * Host errors: ORPO_ERR_ARG for a negative or non-finite eps; otherwise those
+ * of orpo_head_fwd / orpo_head_bwd.  The workspace is orpo_head_workspace_bytes.
+ */
+size_t orpo_head_block_max_elems(int64_t M, int64_t V);
+int orpo_head_fwd_bmax(const void* h_bf16, const void* W_bf16, const int32_t* targets,
+                       const uint8_t* mask, int64_t M, int64_t V, int64_t d, float softcap,
+                       float* logp, float* lse, float* block_max, void* workspace, size_t ws_bytes,
+                       int32_t* status, void* stream);
+int orpo_head_bwd_skip(const void* h_bf16, const void* W_bf16, const int32_t* targets,
+                       const uint8_t* mask, const float* lse, const float* g, const float* block_max,
+                       float eps, int64_t M, int64_t V, int64_t d, float softcap, float* dh,
+                       float* dW, int accumulate_dW, void* workspace, size_t ws_bytes,
+                       int32_t* status, void* stream);
+
 /* Text of a return code or of a set of ORPO_STATUS_* bits (static storage). */
 const char* orpo_status_string(int code);
 

@@ -75,6 +75,13 @@ def load():
     L.orpo_head_fwd_static.restype = ctypes.c_int
     L.orpo_debug_wait_timeout.argtypes = [vp, i64, vp]
     L.orpo_debug_wait_timeout.restype = ctypes.c_int
+    L.orpo_head_block_max_elems.argtypes = [i64, i64]
+    L.orpo_head_block_max_elems.restype = sz
+    L.orpo_head_fwd_bmax.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp, vp, vp, vp, sz, vp, vp]
+    L.orpo_head_fwd_bmax.restype = ctypes.c_int
+    L.orpo_head_bwd_skip.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, i64, i64, i64, f32, vp, vp, ctypes.c_int, vp,
+                                     sz, vp, vp]
+    L.orpo_head_bwd_skip.restype = ctypes.c_int
     L.orpo_profile_start.argtypes = []
     L.orpo_profile_start.restype = ctypes.c_int
     L.orpo_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), ctypes.c_int]
@@ -215,6 +222,58 @@ def orpo_head_bwd(h, W, targets, mask, lse, g, softcap, dh, dW, accumulate_dW, w
                                 workspace.numel(), _ptr(status), _stream(stream)), "orpo_head_bwd")
 
 
+def orpo_head_block_max_elems(M: int, V: int) -> int:
+    return int(load().orpo_head_block_max_elems(M, V))
+
+
+def block_max_shape(M: int, V: int):
+    """[ceil(M / 32), ceil(V / 256)]: the block-max array of the backward skips."""
+    return (-(-M // 32), -(-V // 256))
+
+
+def orpo_head_fwd_bmax(h, W, targets, mask, softcap, logp, lse, block_max, workspace, status, stream=None):
+    """orpo_head_fwd that also writes the block maxima the backward's block skip reads."""
+    M, d = h.shape
+    V = W.shape[0]
+    _dev(h, "h", BF16)
+    _dev(W, "W", BF16, (V, d))
+    _dev(targets, "targets", (torch.int32,), (M,))
+    _dev(mask, "mask", (torch.uint8, torch.bool), (M,))
+    _dev(logp, "logp", (torch.float32,), (M,))
+    _dev(lse, "lse", (torch.float32,), (M,))
+    _dev(block_max, "block_max", (torch.float32,), block_max_shape(M, V))
+    _dev(workspace, "workspace", (torch.uint8,))
+    _dev(status, "status", (torch.int32,))
+    _check(load().orpo_head_fwd_bmax(_ptr(h), _ptr(W), _ptr(targets), _ptr(mask), M, V, d, float(softcap),
+                                     _ptr(logp), _ptr(lse), _ptr(block_max), _ptr(workspace), workspace.numel(),
+                                     _ptr(status), _stream(stream)), "orpo_head_fwd_bmax")
+
+
+def orpo_head_bwd_skip(h, W, targets, mask, lse, g, block_max, eps, softcap, dh, dW, accumulate_dW, workspace,
+                       status, stream=None):
+    """orpo_head_bwd with the backward skips: the coefficient filter at eps, and the block skip when
+    block_max (from orpo_head_fwd_bmax) is given (None: filter alone)."""
+    M, d = h.shape
+    V = W.shape[0]
+    _dev(h, "h", BF16)
+    _dev(W, "W", BF16, (V, d))
+    _dev(targets, "targets", (torch.int32,), (M,))
+    _dev(mask, "mask", (torch.uint8, torch.bool), (M,))
+    _dev(lse, "lse", (torch.float32,), (M,))
+    _dev(g, "g", (torch.float32,), (M,))
+    if block_max is not None:
+        _dev(block_max, "block_max", (torch.float32,), block_max_shape(M, V))
+    _dev(dh, "dh", (torch.float32,), (M, d))
+    if dW is not None:
+        _dev(dW, "dW", (torch.float32,), (V, d))
+    _dev(workspace, "workspace", (torch.uint8,))
+    _dev(status, "status", (torch.int32,))
+    _check(load().orpo_head_bwd_skip(_ptr(h), _ptr(W), _ptr(targets), _ptr(mask), _ptr(lse), _ptr(g),
+                                     _ptr(block_max), float(eps), M, V, d, float(softcap), _ptr(dh), _ptr(dW),
+                                     1 if accumulate_dW else 0, _ptr(workspace), workspace.numel(), _ptr(status),
+                                     _stream(stream)), "orpo_head_bwd_skip")
+
+
 def orpo_head_q_workspace_bytes(M: int, V: int, d: int) -> int:
     return int(load().orpo_head_q_workspace_bytes(M, V, d))
 
@@ -273,7 +332,7 @@ def orpo_debug_wait_timeout(status, limit_ns, stream=None):
     _check(load().orpo_debug_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)), "orpo_debug_wait_timeout")
 
 
-PROFILE_KINDS = 7
+PROFILE_KINDS = 8
 
 
 def orpo_profile_start():
@@ -295,9 +354,13 @@ class OrpoHead:
     entry points in order on the current stream.
     """
 
-    def __init__(self, M: int, V: int, d: int, n_pairs: int, device="cuda"):
+    def __init__(self, M: int, V: int, d: int, n_pairs: int, device="cuda", skip_eps: float = 0.0):
+        """skip_eps > 0 turns on the backward skips (coefficient filter and block skip) at that eps."""
         self.M, self.V, self.d, self.P = M, V, d, n_pairs
+        self.skip_eps = float(skip_eps)
         dev = torch.device(device)
+        self.block_max = (torch.empty(block_max_shape(M, V), dtype=torch.float32, device=dev)
+                          if self.skip_eps > 0 else None)
         self.workspace = torch.empty(orpo_head_workspace_bytes(M, V, d), dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.logp = torch.empty(M, dtype=torch.float32, device=dev)
@@ -309,8 +372,16 @@ class OrpoHead:
         self.dW = torch.empty((V, d), dtype=torch.float32, device=dev)
 
     def step(self, h, W, targets, mask, seq_id, softcap, lam, accumulate_dW=False, stream=None):
-        orpo_head_fwd(h, W, targets, mask, softcap, self.logp, self.lse, self.workspace, self.status, stream)
+        if self.skip_eps > 0:
+            orpo_head_fwd_bmax(h, W, targets, mask, softcap, self.logp, self.lse, self.block_max, self.workspace,
+                               self.status, stream)
+        else:
+            orpo_head_fwd(h, W, targets, mask, softcap, self.logp, self.lse, self.workspace, self.status, stream)
         orpo_loss(self.logp, seq_id, mask, self.P, lam, self.out, self.ell, self.g, self.status, stream)
-        orpo_head_bwd(h, W, targets, mask, self.lse, self.g, softcap, self.dh, self.dW, accumulate_dW,
-                      self.workspace, self.status, stream)
+        if self.skip_eps > 0:
+            orpo_head_bwd_skip(h, W, targets, mask, self.lse, self.g, self.block_max, self.skip_eps, softcap,
+                               self.dh, self.dW, accumulate_dW, self.workspace, self.status, stream)
+        else:
+            orpo_head_bwd(h, W, targets, mask, self.lse, self.g, softcap, self.dh, self.dW, accumulate_dW,
+                          self.workspace, self.status, stream)
         return self.out

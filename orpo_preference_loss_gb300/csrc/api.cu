@@ -120,6 +120,11 @@ size_t wblock_bytes(int64_t M, int64_t V, int64_t d) { return (size_t)wblock_row
 constexpr int kCounters = 4096;
 constexpr size_t kCounterBytes = kCounters * sizeof(int);
 
+// Backward-skip area after the counters: tile list + count, dh / dW k-lists and counts (ints), then
+// the filter's keep flags (bytes).
+constexpr size_t kSkipBytes = 96 << 10;
+static_assert((size_t)kMaxTiles * (5 * sizeof(int) + 1) + 64 <= kSkipBytes, "skip area too small");
+
 // Number of vocabulary splits: minimise (waves of units) x (tiles per unit);
 // ties go to fewer splits (fewer partials to merge).
 int choose_nsplit(int64_t n_mt, int64_t n_vt, int sms) {
@@ -209,13 +214,13 @@ int check_quant(const QuantW* q, int64_t d) {
 // workspace layout (quantised path): [partials | S + counters] then the bf16 W block
 void* wblock_ptr(void* workspace, int64_t M, int64_t V) {
   uintptr_t p = reinterpret_cast<uintptr_t>(align_ws(workspace));
-  p += std::max(partial_bytes(M, kNsplitMaxQ), scratch_bytes(M, V) + kCounterBytes);
+  p += std::max(partial_bytes(M, kNsplitMaxQ), scratch_bytes(M, V) + kCounterBytes + kSkipBytes);
   return reinterpret_cast<void*>((p + 1023) & ~uintptr_t(1023));
 }
 
 int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* targets, const uint8_t* mask,
-                  int64_t M, int64_t V, int64_t d, float softcap, float* logp, float* lse, void* workspace,
-                  size_t ws_bytes, int32_t* status, void* stream) {
+                  int64_t M, int64_t V, int64_t d, float softcap, float* logp, float* lse, float* bmax,
+                  void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
   if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return ORPO_ERR_SHAPE;
   if (M == 0) return ORPO_OK;
   if (!h || (!W && !q) || !targets || !mask || !logp || !lse || !workspace || !status) return ORPO_ERR_NULL;
@@ -247,6 +252,7 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   L.V = (int)V;
   L.softcap = softcap > 0.f ? softcap : 0.f;
   L.status = status;
+  L.bmax = bmax;
   // vocabulary blocks: the whole vocabulary for bf16 W; bounded dequantised blocks otherwise
   const int64_t vb = q ? wblock_rows(M, V, d) : V;
   const int64_t nblocks = cdiv(V, vb);
@@ -278,8 +284,9 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
 }
 
 int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* targets, const uint8_t* mask,
-                  const float* lse, const float* g, int64_t M, int64_t V, int64_t d, float softcap, float* dh,
-                  float* dW, int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
+                  const float* lse, const float* g, const float* bmax, float eps, int64_t M, int64_t V, int64_t d,
+                  float softcap, float* dh, float* dW, int accumulate_dW, void* workspace, size_t ws_bytes,
+                  int32_t* status, void* stream) {
   if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return ORPO_ERR_SHAPE;
   if ((!W && !q) || !status) return ORPO_ERR_NULL;
   if (M > 0 && (!h || !targets || !mask || !lse || !g || !dh || !workspace)) return ORPO_ERR_NULL;
@@ -287,7 +294,7 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
       (M > 0 && (!aligned16(h) || !aligned16(dh) || !aligned16(workspace))))
     return ORPO_ERR_ALIGN;
   if (int e = check_quant(q, d)) return e;
-  if (!isfinite(softcap)) return ORPO_ERR_ARG;
+  if (!isfinite(softcap) || !isfinite(eps) || eps < 0.f) return ORPO_ERR_ARG;
   if (M > 0 && ws_bytes < (q ? orpo_head_q_workspace_bytes(M, V, d) : orpo_head_workspace_bytes(M, V, d)))
     return ORPO_ERR_WORKSPACE;
   int sms = 0;
@@ -301,6 +308,23 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   const BwdBlocks B = bwd_blocks(M, V);
   void* S = align_ws(workspace);
   int* counters = reinterpret_cast<int*>(static_cast<uint8_t*>(S) + scratch_bytes(M, V));
+  // backward skips: plan / index lists in the area after the counters
+  const bool skip = eps > 0.f;
+  SkipPlan P{};
+  {
+    int* a = counters + kCounters;
+    P.list = a;
+    P.count = a + kMaxTiles;
+    P.rowlist = a + kMaxTiles + 16;
+    P.rowcnt = P.rowlist + kMaxTiles;
+    P.collist = P.rowcnt + kMaxTiles;
+    P.colcnt = P.collist + kMaxTiles;
+    P.flags = reinterpret_cast<uint8_t*>(P.colcnt + kMaxTiles);
+    P.g = g, P.mask = mask, P.targets = targets, P.lse = lse, P.bmax = bmax;
+    P.bmax_ld = (int)cdiv(V, kBN);
+    P.M = (int)M, P.V = (int)V, P.status = status;
+    P.thr2 = skip ? log2f(eps) : 0.f;
+  }
   void* Wb = q ? wblock_ptr(workspace, M, V) : nullptr;
   int64_t launch = 0;
   const int64_t sp = scratch_pitch(B);
@@ -354,7 +378,21 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
       R.n_mt = n_mt;
       R.n_vt = n_vt;
       R.grid = (int)std::min<int64_t>((int64_t)n_mt * n_vt, sms);
+      if (skip) {
+        if ((int64_t)n_mt * n_vt > kMaxTiles) return ORPO_ERR_SHAPE;  // cannot happen: Mc * Vc is bounded
+        P.m0 = (int)m0, P.mc = (int)mc, P.v0 = (int)v0, P.vc = (int)vc, P.n_mt = n_mt, P.n_vt = n_vt;
+        if (bmax) {  // block skip: plan the tiles to recompute (and zero the flags)
+          if (launch_skip_plan(P, st) != cudaSuccess) return ORPO_ERR_CUDA;
+          R.list = P.list;
+          R.count = P.count;
+        } else if (cudaMemsetAsync(P.flags, 0, (size_t)n_mt * n_vt, st) != cudaSuccess) {
+          return ORPO_ERR_CUDA;
+        }
+        R.flags = P.flags;
+        R.eps = eps;
+      }
       if (launch_recompute(R, st) != cudaSuccess) return ORPO_ERR_CUDA;
+      if (skip && launch_skip_index(P, st) != cudaSuccess) return ORPO_ERR_CUDA;
 
       GemmClassH cdw{};  // dW[v0 + ..] (+)= S^T h[m0 + ..]
       if (dW) {
@@ -365,6 +403,9 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
         cdw.out_rows = (int)V, cdw.out_cols = (int)d;
         cdw.n_mt = (int)cdiv(vc, kBM), cdw.n_nt = n_nt, cdw.kblocks = (int)cdiv(mc, 64);
         cdw.mt_major = 1;  // CTAs running together share one column slab of S; h stays in L2
+        if (skip) {        // K: the kept row tiles of this 128-column tile's vocabulary tile, 2 k-blocks each
+          cdw.klist = P.collist, cdw.kcnt = P.colcnt, cdw.list_ld = n_mt, cdw.list_shift = 1, cdw.kg_shift = 1;
+        }
       }
       GemmClassH cdh{};  // dh[m0 + ..] (+)= S W[v0 + ..]
       cdh.a_map = 0, cdh.a_mn = 0, cdh.a_mn_base = 0, cdh.a_k_base = 0;
@@ -374,6 +415,9 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
       cdh.out_rows = (int)M, cdh.out_cols = (int)d;
       cdh.n_mt = n_mt, cdh.n_nt = n_nt, cdh.kblocks = (int)cdiv(vc, 64);
       cdh.mt_major = 1;
+      if (skip) {  // K: the kept vocabulary tiles of this row tile, 4 k-blocks each
+        cdh.klist = P.rowlist, cdh.kcnt = P.rowcnt, cdh.list_ld = n_vt, cdh.list_shift = 0, cdh.kg_shift = 2;
+      }
       // longer tiles first
       if (dW && cdw.kblocks >= cdh.kblocks) {
         G.cls[0] = cdw;
@@ -397,28 +441,28 @@ extern "C" {
 
 size_t orpo_head_workspace_bytes(int64_t M, int64_t V, int64_t d) {
   if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return 0;
-  return std::max(partial_bytes(M, kNsplitMax), scratch_bytes(M, V) + kCounterBytes) + 1024;
+  return std::max(partial_bytes(M, kNsplitMax), scratch_bytes(M, V) + kCounterBytes + kSkipBytes) + 1024;
 }
 
 size_t orpo_head_q_workspace_bytes(int64_t M, int64_t V, int64_t d) {
   if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return 0;
-  return std::max(partial_bytes(M, kNsplitMaxQ), scratch_bytes(M, V) + kCounterBytes) + wblock_bytes(M, V, d) +
-         2048;
+  return std::max(partial_bytes(M, kNsplitMaxQ), scratch_bytes(M, V) + kCounterBytes + kSkipBytes) +
+         wblock_bytes(M, V, d) + 2048;
 }
 
 int orpo_head_fwd(const void* h, const void* W, const int32_t* targets, const uint8_t* mask, int64_t M, int64_t V,
                   int64_t d, float softcap, float* logp, float* lse, void* workspace, size_t ws_bytes,
                   int32_t* status, void* stream) {
-  return head_fwd_impl(h, W, nullptr, targets, mask, M, V, d, softcap, logp, lse, workspace, ws_bytes, status,
-                       stream);
+  return head_fwd_impl(h, W, nullptr, targets, mask, M, V, d, softcap, logp, lse, nullptr, workspace, ws_bytes,
+                       status, stream);
 }
 
 int orpo_head_fwd_q(const void* h, const uint8_t* wq, const void* scales, const void* biases, int bits, int group,
                     const int32_t* targets, const uint8_t* mask, int64_t M, int64_t V, int64_t d, float softcap,
                     float* logp, float* lse, void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
   const QuantW q{wq, scales, biases, bits, group};
-  return head_fwd_impl(h, nullptr, &q, targets, mask, M, V, d, softcap, logp, lse, workspace, ws_bytes, status,
-                       stream);
+  return head_fwd_impl(h, nullptr, &q, targets, mask, M, V, d, softcap, logp, lse, nullptr, workspace, ws_bytes,
+                       status, stream);
 }
 
 int orpo_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int64_t M, int32_t n_pairs,
@@ -457,8 +501,8 @@ int orpo_pref_loss(int kind, const float* logp, const int32_t* seq_id, const uin
 int orpo_head_bwd(const void* h, const void* W, const int32_t* targets, const uint8_t* mask, const float* lse,
                   const float* g, int64_t M, int64_t V, int64_t d, float softcap, float* dh, float* dW,
                   int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* status, void* stream) {
-  return head_bwd_impl(h, W, nullptr, targets, mask, lse, g, M, V, d, softcap, dh, dW, accumulate_dW, workspace,
-                       ws_bytes, status, stream);
+  return head_bwd_impl(h, W, nullptr, targets, mask, lse, g, nullptr, 0.f, M, V, d, softcap, dh, dW, accumulate_dW,
+                       workspace, ws_bytes, status, stream);
 }
 
 int orpo_head_bwd_q(const void* h, const uint8_t* wq, const void* scales, const void* biases, int bits, int group,
@@ -466,8 +510,31 @@ int orpo_head_bwd_q(const void* h, const uint8_t* wq, const void* scales, const 
                     int64_t V, int64_t d, float softcap, float* dh, float* dW, int accumulate_dW, void* workspace,
                     size_t ws_bytes, int32_t* status, void* stream) {
   const QuantW q{wq, scales, biases, bits, group};
-  return head_bwd_impl(h, nullptr, &q, targets, mask, lse, g, M, V, d, softcap, dh, dW, accumulate_dW, workspace,
-                       ws_bytes, status, stream);
+  return head_bwd_impl(h, nullptr, &q, targets, mask, lse, g, nullptr, 0.f, M, V, d, softcap, dh, dW,
+                       accumulate_dW, workspace, ws_bytes, status, stream);
+}
+
+size_t orpo_head_block_max_elems(int64_t M, int64_t V) {
+  if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows) return 0;
+  return (size_t)cdiv(M, 32) * (size_t)cdiv(V, kBN);
+}
+
+int orpo_head_fwd_bmax(const void* h, const void* W, const int32_t* targets, const uint8_t* mask, int64_t M,
+                       int64_t V, int64_t d, float softcap, float* logp, float* lse, float* block_max, void* workspace,
+                       size_t ws_bytes, int32_t* status, void* stream) {
+  if (M > 0 && !block_max) return ORPO_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(block_max) & 3u) return ORPO_ERR_ALIGN;
+  return head_fwd_impl(h, W, nullptr, targets, mask, M, V, d, softcap, logp, lse, block_max, workspace, ws_bytes,
+                       status, stream);
+}
+
+int orpo_head_bwd_skip(const void* h, const void* W, const int32_t* targets, const uint8_t* mask, const float* lse,
+                       const float* g, const float* block_max, float eps, int64_t M, int64_t V, int64_t d,
+                       float softcap, float* dh, float* dW, int accumulate_dW, void* workspace, size_t ws_bytes,
+                       int32_t* status, void* stream) {
+  if (reinterpret_cast<uintptr_t>(block_max) & 3u) return ORPO_ERR_ALIGN;
+  return head_bwd_impl(h, W, nullptr, targets, mask, lse, g, block_max, eps, M, V, d, softcap, dh, dW,
+                       accumulate_dW, workspace, ws_bytes, status, stream);
 }
 
 int orpo_debug_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int a_mn_major,

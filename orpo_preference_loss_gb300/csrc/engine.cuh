@@ -119,10 +119,22 @@ struct Operand {
   int k0;        // first K coordinate of k-block 0
 };
 
+// kblocks k-blocks of BK, in order.  Dense (klist == nullptr): k-block i is i.  Sparse: k-block i is
+// (klist[i >> kg_shift] << kg_shift) + (i & ((1 << kg_shift) - 1)), i.e. the list names groups of
+// 2^kg_shift consecutive k-blocks (ascending; only the last group may be cut short by kblocks).  A tile
+// with kblocks == 0 issues no loads and no MMAs and takes no accumulator; the kernel's epilogue
+// handles it without waiting on the accumulator.
 struct TileOps {
   Operand a, b;
   int kblocks;
+  const int* klist = nullptr;
+  int kg_shift = 0;
 };
+
+__device__ __forceinline__ int tile_kblock(const TileOps& t, int i) {
+  if (t.klist == nullptr) return i;
+  return (__ldg(t.klist + (i >> t.kg_shift)) << t.kg_shift) + (i & ((1 << t.kg_shift) - 1));
+}
 
 __device__ __forceinline__ uint8_t* smem_base_aligned() {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -196,7 +208,8 @@ __device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* sme
     const int len = sched.unit_len(u);
     for (int j = 0; ok && j < len; ++j) {
       const TileOps t = sched.tile(u, j);
-      for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
+      for (int i = 0; i < t.kblocks; ++i, ++it) {
+        const int kb = tile_kblock(t, i);
         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
         if (!wait_phase(ctl, &ctl->empty[s], ph ^ 1u, status)) {
           ok = false;
@@ -231,9 +244,11 @@ __device__ void mma_role(const Sched& sched, const Feed& feed, uint8_t* smem, Sm
     const int u = feed_consume(feed, ctl, i, status, false);
     if (u < 0) break;
     const int len = sched.unit_len(u);
-    for (int j = 0; ok && j < len; ++j, ++tcount) {
+    for (int j = 0; ok && j < len; ++j) {
       const TileOps t = sched.tile(u, j);
+      if (t.kblocks == 0) continue;  // empty tile: no accumulator (the epilogue knows)
       const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
+      ++tcount;
       if (!wait_phase(ctl, &ctl->acc_empty[buf], aph ^ 1u, status)) {
         ok = false;
         break;

@@ -25,11 +25,15 @@ struct RecSched {
   const CUtensorMap* mh;
   const CUtensorMap* mw;
   int m0, v0, n_mt, n_vt, kblocks;
-  int w_row0;  // row of the W map that holds vocabulary column v0
-  __device__ int num_units() const { return n_mt * n_vt; }
+  int w_row0;        // row of the W map that holds vocabulary column v0
+  const int* list;   // backward skips: the tiles to compute (vt * n_mt + mt, ascending), or nullptr for all
+  const int* count;  // number of entries of list
+  __device__ int num_units() const { return list ? __ldg(count) : n_mt * n_vt; }
+  __device__ int tile_index(int u) const { return list ? __ldg(list + u) : u; }
   __device__ int unit_len(int) const { return 1; }
   __device__ TileOps tile(int u, int) const {
-    const int vt = u / n_mt, mt = u - vt * n_mt;
+    const int x = tile_index(u);
+    const int vt = x / n_mt, mt = x - vt * n_mt;
     TileOps t;
     t.a = Operand{mh, 0, m0 + mt * BM, 0};
     t.b = Operand{mw, 0, w_row0 + vt * BN, 0};
@@ -46,6 +50,8 @@ struct RecArgs {
   int M, V;
   float softcap;
   int32_t* status;
+  float eps;       // coefficient filter threshold (filter instances only)
+  uint8_t* flags;  // [n_mt][n_vt] of the block: set to 1 for a tile the filter keeps (filter instances only)
 };
 
 // dZ for 32 accumulator values of one row starting at vocabulary column col0;
@@ -57,9 +63,9 @@ struct RecArgs {
 constexpr int kCapOff = 0, kCapExp = 1, kCapHybrid = 2;  // softcap forms, as in the forward
 constexpr float kCapExpMax = 64.f;
 
-template <int cap>
+template <int cap, bool kFilter>
 __device__ __forceinline__ void dz_chunk(const uint32_t (&r)[32], int col0, int V, int y, float gval, float lse2,
-                                         float inv_c, float cl2, uint32_t* w) {
+                                         float inv_c, float cl2, uint32_t* w, float& amax) {
   float dz[32], sl[32];
   if constexpr (cap == kCapExp) {
     const float K = 2.f * kLog2e * inv_c, A = cl2 - lse2, B2 = 2.f * cl2;
@@ -117,11 +123,18 @@ __device__ __forceinline__ void dz_chunk(const uint32_t (&r)[32], int col0, int 
     for (int i = 0; i < 32; ++i)
       if (col0 + i >= V) dz[i] = 0.f;
   }
+  if constexpr (kFilter) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(dz[i]));
+  }
 #pragma unroll
   for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(dz[2 * i], dz[2 * i + 1]);
 }
 
-template <int cap>
+// kFilter: the coefficient filter of the backward skips ("Steel flash-CCE — handoff" §E).  A tile
+// is kept (flags = 1) when some row with g != 0 has |dZ| >= eps |g|, i.e. an entry of
+// (onehot - p) sech^2 reaches eps; the dh / dW GEMMs read only kept tiles.
+template <int cap, bool kFilter>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     rec_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mw,
                const __grid_constant__ CUtensorMap ms, RecSched sched, RecArgs p) {
@@ -142,7 +155,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (uint32_t i = 0;; ++i, ++tcount) {
       const int u = feed_consume(feed, ctl, i, p.status, true);
       if (u < 0) break;
-      const int vt = u / sched.n_mt, mt = u - vt * sched.n_mt;
+      const int x = sched.tile_index(u);
+      const int vt = x / sched.n_mt, mt = x - vt * sched.n_mt;
       const int srow = mt * BM + 32 * q;  // first scratch row of this warp
       const int row = sched.m0 + srow + lane;
       float gval = 0.f, lse2 = 0.f;
@@ -160,6 +174,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t taddr;
       if (!epi_acquire(ctl, tmem_base, tcount, warp, p.status, &taddr)) break;
       const int vcol0 = sched.v0 + vt * BN;  // global vocabulary column of the tile
+      float amax = 0.f;                       // largest |dZ| of this row in the tile (filter)
       uint32_t ra[32], rb[32];
       if (!warp_zero) tmem_ld32(taddr, ra);
 #pragma unroll 1
@@ -171,10 +186,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else {
           tmem_ld_wait(ra);
           tmem_ld32(taddr + gi * 64 + 32, rb);
-          dz_chunk<cap>(ra, vcol0 + gi * 64, p.V, y, gval, lse2, inv_c, cl2, w);
+          dz_chunk<cap, kFilter>(ra, vcol0 + gi * 64, p.V, y, gval, lse2, inv_c, cl2, w, amax);
           tmem_ld_wait(rb);
           if (gi + 1 < BN / 64) tmem_ld32(taddr + gi * 64 + 64, ra);
-          dz_chunk<cap>(rb, vcol0 + gi * 64 + 32, p.V, y, gval, lse2, inv_c, cl2, w + 16);
+          dz_chunk<cap, kFilter>(rb, vcol0 + gi * 64 + 32, p.V, y, gval, lse2, inv_c, cl2, w + 16, amax);
         }
         const uint32_t box = staging + (nstore & 1u) * BOX_BYTES;
         if (lane == 0) bulk_wait_group_read<1>();  // the store that used this buffer has read it
@@ -190,6 +205,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++nstore;
       }
       epi_release(ctl, tcount);
+      if constexpr (kFilter) {
+        const bool keep = gval != 0.f && amax >= p.eps * fabsf(gval);
+        if (__any_sync(0xffffffffu, keep) && lane == 0) p.flags[mt * sched.n_vt + vt] = 1;
+      }
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
@@ -204,6 +223,11 @@ struct GemmClass {
   int out_rows, out_cols;
   int n_mt, n_nt, kblocks;
   int mt_major;
+  // sparse K (backward skips): list (mt >> list_shift) of k-block groups, list_ld entries apart, with
+  // its k-block count in kcnt; groups are 2^kg_shift k-blocks.  klist == nullptr: dense, kblocks.
+  const int* klist;
+  const int* kcnt;
+  int list_ld, list_shift, kg_shift;
 };
 
 struct GemmSched {
@@ -252,6 +276,12 @@ struct GemmSched {
     t.a = Operand{map(c.a_map), c.a_mn, c.a_mn_base + mt * BM, c.a_k_base};
     t.b = Operand{map(c.b_map), c.b_mn, c.b_mn_base + nt * BN, c.b_k_base};
     t.kblocks = c.kblocks;
+    if (c.klist != nullptr) {
+      const int li = mt >> c.list_shift;
+      t.klist = c.klist + (size_t)li * c.list_ld;
+      t.kblocks = __ldg(c.kcnt + li);
+      t.kg_shift = c.kg_shift;
+    }
     return t;
   }
 };
@@ -276,7 +306,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* stage_ptr = smem + SMEM_STAGING_OFF + (warp - 2) * STAGING_PER_WARP;
     const uint32_t staging = smem_u32(stage_ptr);
     uint32_t tcount = 0, nstore = 0;
-    for (uint32_t i = 0;; ++i, ++tcount) {
+    for (uint32_t i = 0;; ++i) {
       const int u = feed_consume(feed, ctl, i, status, true);
       if (u < 0) break;
       int k, mt, nt;
@@ -285,6 +315,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const CUtensorMap* out = sched.map(c.out_map);
       const int orow = c.out_row_base + mt * BM + 32 * q;
       const int ocol0 = c.out_col_base + nt * BN;
+      if (sched.tile(u, 0).kblocks == 0) {
+        // empty sparse tile: nothing to add; a first (store) write still owes the tile its zeros
+        if (!c.reduce && orow < c.out_rows) {
+#pragma unroll 1
+          for (int ch = 0; ch < BN / 32; ++ch) {
+            const int col = ocol0 + ch * 32;
+            if (col >= c.out_cols) break;
+            const uint32_t box = staging + (nstore & 1u) * BOX_BYTES;
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            const uint32_t zero[32] = {};
+            stage_row_f32(box, lane, zero);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(out, stage_ptr + (nstore & 1u) * BOX_BYTES, col, orow);
+              bulk_commit_group();
+            }
+            ++nstore;
+          }
+        }
+        continue;
+      }
       uint32_t taddr;
       if (!epi_acquire(ctl, tmem_base, tcount, warp, status, &taddr)) break;
       if (orow < c.out_rows) {
@@ -325,6 +378,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       epi_release(ctl, tcount);
+      ++tcount;
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
@@ -334,24 +388,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }  // namespace
 
 namespace {
-template <int cap>
+template <int cap, bool kFilter>
 cudaError_t launch_rec_kernel(const RecLaunch& L, cudaStream_t st) {
   static int smem_set[64] = {0};
-  if (cudaError_t e = opt_in_smem(rec_kernel<cap>, SMEM_TOTAL, smem_set)) return e;
-  RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks, L.w_row0};
-  RecArgs a{L.targets, L.mask, L.lse, L.g, L.M, L.V, L.softcap, L.status};
+  if (cudaError_t e = opt_in_smem(rec_kernel<cap, kFilter>, SMEM_TOTAL, smem_set)) return e;
+  RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks, L.w_row0, L.list, L.count};
+  RecArgs a{L.targets, L.mask, L.lse, L.g, L.M, L.V, L.softcap, L.status, L.eps, L.flags};
   prof_begin(K_REC, st);
-  rec_kernel<cap><<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, L.ms_store, sched, a);
+  rec_kernel<cap, kFilter><<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, L.ms_store, sched, a);
   prof_end(K_REC, st);
   return cudaGetLastError();
+}
+
+template <bool kFilter>
+cudaError_t launch_rec_cap(const RecLaunch& L, cudaStream_t st) {
+  const int cap = L.softcap > 0.f ? (L.softcap <= kCapExpMax ? kCapExp : kCapHybrid) : kCapOff;
+  return cap == kCapExp      ? launch_rec_kernel<kCapExp, kFilter>(L, st)
+         : cap == kCapHybrid ? launch_rec_kernel<kCapHybrid, kFilter>(L, st)
+                             : launch_rec_kernel<kCapOff, kFilter>(L, st);
 }
 }  // namespace
 
 cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st) {
-  const int cap = L.softcap > 0.f ? (L.softcap <= kCapExpMax ? kCapExp : kCapHybrid) : kCapOff;
-  return cap == kCapExp      ? launch_rec_kernel<kCapExp>(L, st)
-         : cap == kCapHybrid ? launch_rec_kernel<kCapHybrid>(L, st)
-                             : launch_rec_kernel<kCapOff>(L, st);
+  return L.flags ? launch_rec_cap<true>(L, st) : launch_rec_cap<false>(L, st);
 }
 
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
@@ -361,9 +420,10 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
   for (int i = 0; i < 6; ++i) sched.maps[i] = nullptr;
   for (int k = 0; k < 2; ++k) {
     const GemmClassH& h = L.cls[k];
-    sched.cls[k] = GemmClass{h.a_map,   h.a_mn,         h.a_mn_base,    h.a_k_base, h.b_map,    h.b_mn,
-                             h.b_mn_base, h.b_k_base,   h.out_map,      h.out_row_base, h.out_col_base, h.reduce,
-                             h.out_rows,  h.out_cols,   h.n_mt,         h.n_nt,     h.kblocks,  h.mt_major};
+    sched.cls[k] = GemmClass{h.a_map,     h.a_mn,      h.a_mn_base,  h.a_k_base,     h.b_map,        h.b_mn,
+                             h.b_mn_base, h.b_k_base,  h.out_map,    h.out_row_base, h.out_col_base, h.reduce,
+                             h.out_rows,  h.out_cols,  h.n_mt,       h.n_nt,         h.kblocks,      h.mt_major,
+                             h.klist,     h.kcnt,      h.list_ld,    h.list_shift,   h.kg_shift};
   }
   prof_begin(kind, st);
   gemm_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.maps[0], L.maps[1], L.maps[2], L.maps[3], L.maps[4],

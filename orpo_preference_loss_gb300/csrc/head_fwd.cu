@@ -63,6 +63,9 @@ struct FwdArgs {
   int32_t* status;
   int col0;    // vocabulary column of row 0 of the W map (0 unless W is a block of the vocabulary)
   int split0;  // index of this launch's first split in the partial arrays
+  float* bmax;   // optional block maxima [ceil(M/32), bmax_ld]: max of x over a 32-row group's mask != 0
+                 // rows and one 256-column vocabulary tile (-inf for a group with no such row)
+  int bmax_ld;   // ceil(V / 256)
 };
 
 // Per-row online softmax state of one epilogue thread, base-2 units.
@@ -83,7 +86,7 @@ constexpr float kCapExpMax = 64.f;
 // x = z~ log2(e) (base-2 units), z~ = c tanh(z / c) with the softcap on, else z.
 template <int cap>
 __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, int V, int y, float inv_c, float cl2,
-                                           RowState& st, float* tgt_slot) {
+                                           RowState& st, float* tgt_slot, float& tmax) {
   if (col0 >= V) return;
   float x[32];
   if constexpr (cap == kCapExp) {
@@ -133,7 +136,9 @@ __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, in
     m2 = fmaxf(m2, fmaxf(x[i + 4], x[i + 5]));
     m3 = fmaxf(m3, fmaxf(x[i + 6], x[i + 7]));
   }
-  const float mnew = fmaxf(st.m, fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
+  const float cmax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+  tmax = fmaxf(tmax, cmax);
+  const float mnew = fmaxf(st.m, cmax);
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
   for (int i = 0; i < 32; i += 4) {
@@ -171,8 +176,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (u < 0) break;
       const int s = sched.split_of(u), mt = sched.mt_of(u);
       const int row = mt * BM + 32 * q + lane;
+      const bool supervised = row < p.M && p.mask[row] != 0;
+      const int grp = mt * (BM / 32) + q;  // this warp's 32-row group
       int y = -1;
-      if (row < p.M && p.mask[row] != 0) y = p.targets[row];
+      if (supervised) y = p.targets[row];
       float* tgt_slot = p.tgt + (row < p.M ? row : 0);
       RowState st{-INFINITY, 0.f};
       const int len = sched.unit_len(u);
@@ -182,17 +189,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!epi_acquire(ctl, tmem_base, tcount, warp, p.status, &taddr)) return;
         const int col_base = p.col0 + (vt0 + j) * BN;
         uint32_t ra[32], rb[32];
+        float tmax = -INFINITY;
         tmem_ld32(taddr, ra);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; c += 2) {
           tmem_ld_wait(ra);
           tmem_ld32(taddr + (c + 1) * 32, rb);
-          fold_chunk<cap>(ra, col_base + c * 32, p.V, y, inv_c, cl2, st, tgt_slot);
+          fold_chunk<cap>(ra, col_base + c * 32, p.V, y, inv_c, cl2, st, tgt_slot, tmax);
           tmem_ld_wait(rb);
           if (c + 2 < BN / 32) tmem_ld32(taddr + (c + 2) * 32, ra);
-          fold_chunk<cap>(rb, col_base + (c + 1) * 32, p.V, y, inv_c, cl2, st, tgt_slot);
+          fold_chunk<cap>(rb, col_base + (c + 1) * 32, p.V, y, inv_c, cl2, st, tgt_slot, tmax);
         }
         epi_release(ctl, tcount);
+        if (p.bmax != nullptr) {
+          float v = supervised ? tmax : -INFINITY;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+          if (lane == 0 && grp * 32 < p.M) p.bmax[(size_t)grp * p.bmax_ld + col_base / BN] = v;
+        }
       }
       if (row < p.Mpad) {  // pair mode pads an odd tile count with one empty tile
         p.part_m[(size_t)(p.split0 + s) * p.Mpad + row] = st.m;
@@ -235,7 +249,8 @@ cudaError_t launch_fwd_kernel(const FwdLaunch& L, cudaStream_t st) {
   if (cudaError_t e = opt_in_smem(fwd_kernel<cap, kPair>, SMEM_TOTAL, smem_set)) return e;
   const int n_mt = kPair ? (L.n_mt + 1) & ~1 : L.n_mt;
   FwdSched sched{nullptr, nullptr, n_mt, L.nsplit, L.n_vt, L.kblocks, 0, 0};
-  FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M, L.Mpad, L.V, L.softcap, L.status, L.col0, L.split0};
+  FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M,      L.Mpad,
+            L.V,       L.softcap, L.status, L.col0, L.split0, L.bmax, (L.V + BN - 1) / BN};
   cudaError_t e = cudaSuccess;
   prof_begin(K_FWD, st);
   if constexpr (kPair) {

@@ -20,7 +20,7 @@ inline cudaError_t opt_in_smem(Kernel kernel, int bytes, int (&done)[64]) {
 }
 
 // ---- launch timing (profile.cu); no-ops unless orpo_profile_start() was called
-enum KernelKind { K_FWD = 0, K_MERGE, K_LOSS, K_REC, K_GEMM, K_DEBUG, K_DEQUANT, K_NKINDS };
+enum KernelKind { K_FWD = 0, K_MERGE, K_LOSS, K_REC, K_GEMM, K_DEBUG, K_DEQUANT, K_SKIP, K_NKINDS };
 void prof_begin(int kind, cudaStream_t st);
 void prof_end(int kind, cudaStream_t st);
 
@@ -30,6 +30,7 @@ constexpr int kBN = 256;          // columns per accumulator tile
 constexpr int kNsplitMax = 64;    // most vocabulary splits of the forward
 constexpr int64_t kMcMax = 16384; // rows per backward block
 constexpr int64_t kScratchBudget = 256ll << 20;  // bytes of the bf16 dZ block
+constexpr int kMaxTiles = (int)(kScratchBudget / 2 / (kBM * kBN));  // 128 x 256 tiles in one dZ block
 
 // ---- forward
 struct FwdLaunch {
@@ -48,6 +49,7 @@ struct FwdLaunch {
   int col0 = 0;    // vocabulary column of row 0 of mw
   int split0 = 0;  // first split index this launch writes
   int pair = 0;    // 1: 2-CTA clusters share W tiles (mw box {64,128}; grid = 2 x clusters; n_mt padded to even)
+  float* bmax = nullptr;  // optional block maxima [ceil(M/32), ceil(V/256)] (base-2 softcapped logits)
 };
 int forward_pair_clusters();  // co-resident 2-CTA clusters of the forward kernel (0: pair mode unavailable)
 cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st);  // logits kernel + merge of L.nsplit splits
@@ -67,8 +69,35 @@ struct RecLaunch {
   int32_t* status;
   int grid;
   int w_row0;  // row of mw holding vocabulary column m0's block start v0 (v0 itself unless W is a block copy)
+  // backward skips
+  const int* list = nullptr;   // tiles to compute (vt * n_mt + mt, ascending) and their count, or all tiles
+  const int* count = nullptr;
+  uint8_t* flags = nullptr;    // coefficient filter: [n_mt][n_vt] keep flags (zeroed), or nullptr for no filter
+  float eps = 0.f;
 };
 cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st);
+
+// ---- backward skips (skip.cu): per (row block, vocabulary block), tiles of 128 x 256
+struct SkipPlan {
+  const float* g;
+  const uint8_t* mask;
+  const int32_t* targets;
+  const float* lse;
+  const float* bmax;  // forward block maxima [ceil(M/32)][bmax_ld], base 2; nullptr: no block skip
+  int bmax_ld;
+  int m0, mc, v0, vc, n_mt, n_vt, M, V;
+  float thr2;         // log2(eps)
+  int* list;          // [kMaxTiles] tiles to recompute (vt * n_mt + mt, ascending) and their count
+  int* count;
+  uint8_t* flags;     // [n_mt][n_vt] keep flags of the coefficient filter
+  int32_t* status;
+  int* rowlist;       // [n_mt][n_vt] kept vocabulary tiles per row tile (dh GEMM), rowcnt[n_mt] k-blocks
+  int* rowcnt;
+  int* collist;       // [n_vt][n_mt] kept row tiles per vocabulary tile (dW GEMM), colcnt[n_vt] k-blocks
+  int* colcnt;
+};
+cudaError_t launch_skip_plan(const SkipPlan& P, cudaStream_t st);   // zeroes flags; lists the tiles to recompute
+cudaError_t launch_skip_index(const SkipPlan& P, cudaStream_t st);  // GEMM k-lists from the filter's flags
 
 // ---- quantised head: affine group dequantisation of W rows [v0, v0 + rows) into bf16 [rows, d]
 cudaError_t launch_dequant(const uint8_t* wq, const void* scales, const void* biases, int bits, int group,
@@ -82,6 +111,11 @@ struct GemmClassH {
   int out_rows, out_cols;  // valid extent of the output tensor
   int n_mt, n_nt, kblocks;
   int mt_major;
+  // sparse K (backward skips): per list index (mt >> list_shift), ascending groups of 2^kg_shift
+  // k-blocks at klist + index * list_ld and their k-block count kcnt[index]; nullptr: dense
+  const int* klist = nullptr;
+  const int* kcnt = nullptr;
+  int list_ld = 0, list_shift = 0, kg_shift = 0;
 };
 struct GemmLaunch {
   CUtensorMap maps[6];

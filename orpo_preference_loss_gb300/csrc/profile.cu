@@ -33,8 +33,8 @@ cudaEvent_t take_event() {
   return e;
 }
 
-const char* kNames[K_NKINDS] = {"fwd_logits", "fwd_merge",  "orpo_loss", "bwd_recompute",
-                                "bwd_grad_gemm", "debug_gemm", "dequant"};
+const char* kNames[K_NKINDS] = {"fwd_logits",    "fwd_merge",  "orpo_loss", "bwd_recompute",
+                                "bwd_grad_gemm", "debug_gemm", "dequant",   "bwd_skip_plan"};
 
 }  // namespace
 

@@ -100,9 +100,35 @@ def test_status_strings(lib):
 def test_workspace_is_flat_in_M(lib):
     V, d = 262144, 2560
     base = lib.orpo_head_workspace_bytes(16384, V, d)
-    assert base <= (258 << 20) + (16 << 10) + 1024   # dZ block (padded pitch) + GEMM unit counters
+    # dZ block (padded pitch) + GEMM unit counters + the backward skips' tile lists
+    assert base <= (258 << 20) + (16 << 10) + (96 << 10) + 1024
     for M in (16384, 20000, 65536, 131072):
         assert lib.orpo_head_workspace_bytes(M, V, d) == base
     # far below any [M, V] buffer: 8192 x 262144 fp32 logits would be 8 GiB
     assert lib.orpo_head_workspace_bytes(8192, V, d) < (8192 * V * 4) // 16
     assert lib.orpo_head_workspace_bytes(-1, V, d) == 0
+
+
+def test_skip_host_checks(lib):
+    assert lib.orpo_head_block_max_elems(100, 1000) == 4 * 4
+    assert lib.orpo_head_block_max_elems(8192, 262144) == 256 * 1024
+    assert lib.orpo_head_block_max_elems(-1, 10) == 0
+    assert orpo.block_max_shape(100, 1000) == (4, 4)
+
+    def fwd_bm(bm=FAKE, M=64):
+        return lib.orpo_head_fwd_bmax(FAKE, FAKE, FAKE, FAKE, M, 128, 64, 0.0, FAKE, FAKE, bm, FAKE, 1 << 30, FAKE,
+                                      None)
+
+    assert fwd_bm(bm=None) == ERR_NULL
+    assert fwd_bm(bm=ctypes.c_void_p(0x10002)) == ERR_ALIGN
+    assert fwd_bm(M=-1) == ERR_SHAPE
+
+    def bwd_skip(eps=1e-5, bm=FAKE, ws=1 << 30):
+        return lib.orpo_head_bwd_skip(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, bm, eps, 64, 128, 64, 0.0, FAKE, FAKE, 0,
+                                      FAKE, ws, FAKE, None)
+
+    assert bwd_skip(eps=-1e-5) == ERR_ARG
+    assert bwd_skip(eps=float("nan")) == ERR_ARG
+    assert bwd_skip(eps=float("inf")) == ERR_ARG
+    assert bwd_skip(bm=ctypes.c_void_p(0x10002)) == ERR_ALIGN
+    assert bwd_skip(ws=8) == ERR_WS

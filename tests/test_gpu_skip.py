@@ -1,0 +1,164 @@
+"""Backward skips on the GPU ("Steel flash-CCE — handoff" §E; "Training — design" §5.1):
+the forward's block maxima against the oracle, the coefficient filter against the
+oracle's filtered gradient, the block skip (which must leave the filtered result
+unchanged, bit for bit), the limits of eps, and multi-block runs checked on sampled
+row and vocabulary tiles."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import orpo_preference_loss_gb300 as orpo
+import workloads
+from gpu_helpers import GRAD_RELFRO, LOGP_ATOL, dev, f64, gpu_backward, gpu_forward, relfro, status_tensor, \
+    to_dev, workspace
+
+pytestmark = pytest.mark.gpu
+
+LOG2E = 1.4426950408889634
+
+
+def fwd_bmax(t, M, V, d, softcap):
+    logp = torch.full((M,), float("nan"), dtype=torch.float32, device=dev())
+    lse = torch.full((M,), float("nan"), dtype=torch.float32, device=dev())
+    bm = torch.full(orpo.block_max_shape(M, V), float("nan"), dtype=torch.float32, device=dev())
+    st = status_tensor()
+    orpo.orpo_head_fwd_bmax(t["h"], t["W"], t["targets"], t["mask"], softcap, logp, lse, bm, workspace(M, V, d), st)
+    torch.cuda.synchronize()
+    return logp.cpu().numpy(), lse.cpu().numpy(), bm, int(st.item())
+
+
+def bwd_skip(t, lse_np, g_np, bm, eps, M, V, d, softcap, dW_init=None, accumulate=False, with_dW=True):
+    lse = torch.from_numpy(np.asarray(lse_np, dtype=np.float32)).to(dev())
+    g = torch.from_numpy(np.asarray(g_np, dtype=np.float32)).to(dev())
+    dh = torch.full((M, d), float("nan"), dtype=torch.float32, device=dev())
+    dW = None
+    if with_dW:
+        dW = (torch.full((V, d), float("nan"), dtype=torch.float32, device=dev()) if dW_init is None
+              else torch.from_numpy(np.asarray(dW_init, dtype=np.float32)).to(dev()))
+    st = status_tensor()
+    orpo.orpo_head_bwd_skip(t["h"], t["W"], t["targets"], t["mask"], lse, g, bm, eps, softcap, dh, dW, accumulate,
+                            workspace(M, V, d), st)
+    torch.cuda.synchronize()
+    return dh.cpu().numpy(), (dW.cpu().numpy() if with_dW else None), int(st.item())
+
+
+def orpo_g(w, logp):
+    return oracle.orpo_loss(logp, w.seq_id, w.mask, w.n_pairs, w.lam).g
+
+
+@pytest.mark.parametrize("name,M,V,d,softcap", [("tiny", 300, 1000, 72, 0.0), ("e4b_sharp", 384, 4196, 128, 30.0),
+                                                ("tiny", 97, 300, 64, 30.0)])
+def test_block_max_matches_oracle(name, M, V, d, softcap):
+    w = workloads.make(name, M=M, d=d, V=V)
+    if w.M > 64:
+        w.mask[32:64] = 0                      # a whole 32-row group unsupervised: -inf
+    t = to_dev(w)
+    logp, lse, bm, st = fwd_bmax(t, w.M, w.V, w.d, softcap)
+    assert st == 0
+    ref = oracle.head_block_max(f64(w.h), f64(w.W), w.mask, softcap)
+    got = bm.cpu().numpy()
+    assert got.shape == ref.shape
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref))
+    fin = np.isfinite(ref)
+    assert np.max(np.abs(got[fin] - ref[fin])) < LOGP_ATOL * LOG2E
+    # the same logp / lse as the plain forward, bit for bit
+    logp0, lse0, st0 = gpu_forward(t, w.M, w.V, w.d, softcap)
+    assert st0 == 0 and np.array_equal(logp, logp0) and np.array_equal(lse, lse0)
+
+
+# Inputs where the filter matters and the gradient stays well conditioned in fp32: with the sharp
+# recipe uncapped, 1 - p(target) falls to ~2e-5 and the fp32 logits' rounding alone moves the target
+# coefficient g (1 - p) by several percent, filter or not.
+@pytest.mark.parametrize("name,M,V,d,softcap,eps", [("e4b_sharp", 512, 65536, 256, 30.0, 1e-5),
+                                                    ("e4b", 512, 65536, 256, 0.0, 3e-3)])
+def test_skip_matches_filtered_oracle(name, M, V, d, softcap, eps):
+    w = workloads.make(name, M=M, d=d, V=V)
+    h, W = f64(w.h), f64(w.W)
+    logp_r, lse_r = oracle.head_forward(h, W, w.targets, w.mask, softcap)
+    g = orpo_g(w, logp_r)
+    t = to_dev(w)
+    _, lse, bm, st = fwd_bmax(t, w.M, w.V, w.d, softcap)
+    assert st == 0 and np.max(np.abs(lse - lse_r)) < LOGP_ATOL
+    lse32, g32 = lse_r.astype(np.float32), g.astype(np.float32)
+    dh, dW, st = bwd_skip(t, lse32, g32, bm, eps, w.M, w.V, w.d, softcap)
+    assert st == 0
+    rdh, rdW = oracle.head_backward(h, W, w.targets, w.mask, lse32, g32, softcap, filter_eps=eps)
+    edh, edW = oracle.head_backward(h, W, w.targets, w.mask, lse32, g32, softcap)
+    assert relfro(dh, rdh) < GRAD_RELFRO and relfro(dW, rdW) < GRAD_RELFRO
+    # the inputs make the filter matter: the filtered gradient is far from the exact one, so
+    # matching it means the kept and dropped tiles were chosen as the oracle chose them
+    assert relfro(rdh, edh) > 3 * GRAD_RELFRO
+    # the block skip changes no bit of the filtered result
+    dh1, dW1, st1 = bwd_skip(t, lse32, g32, None, eps, w.M, w.V, w.d, softcap)
+    assert st1 == 0 and np.array_equal(dh, dh1) and np.array_equal(dW, dW1)
+
+
+def test_zero_eps_is_the_dense_backward():
+    w = workloads.make("tiny")
+    t = to_dev(w)
+    logp, lse, bm, st = fwd_bmax(t, w.M, w.V, w.d, 30.0)
+    g = orpo_g(w, logp.astype(np.float64))
+    dh0, dW0, st0 = gpu_backward(t, lse, g, w.M, w.V, w.d, 30.0)
+    dh1, dW1, st1 = bwd_skip(t, lse, g, bm, 0.0, w.M, w.V, w.d, 30.0)
+    assert st0 == 0 and st1 == 0
+    assert np.array_equal(dh0, dh1) and np.array_equal(dW0, dW1)
+
+
+@pytest.mark.parametrize("use_bmax", [False, True])
+def test_eps_above_every_coefficient_drops_everything(use_bmax):
+    # |onehot - p| sech^2 <= 1 < 2: every tile is empty, and the first writes still store zeros
+    w = workloads.make("small")
+    t = to_dev(w)
+    logp, lse, bm, st = fwd_bmax(t, w.M, w.V, w.d, 0.0)
+    g = orpo_g(w, logp.astype(np.float64))
+    dh, dW, st = bwd_skip(t, lse, g, bm if use_bmax else None, 2.0, w.M, w.V, w.d, 0.0)
+    assert st == 0 and not dh.any() and not dW.any()
+    init = np.random.default_rng(1).standard_normal((w.V, w.d)).astype(np.float32)
+    _, dW2, st = bwd_skip(t, lse, g, bm if use_bmax else None, 2.0, w.M, w.V, w.d, 0.0, dW_init=init,
+                          accumulate=True)
+    assert st == 0 and np.array_equal(dW2, init)
+
+
+def test_accumulate_and_frozen_head_with_skips():
+    w = workloads.make("e4b_sharp", M=512, d=256, V=65536)   # about half the tiles dropped
+    t = to_dev(w)
+    logp, lse, bm, st = fwd_bmax(t, w.M, w.V, w.d, 30.0)
+    g = orpo_g(w, logp.astype(np.float64))
+    dh, dW, st = bwd_skip(t, lse, g, bm, 1e-5, w.M, w.V, w.d, 30.0)
+    init = np.random.default_rng(2).standard_normal((w.V, w.d)).astype(np.float32)
+    dh2, dW2, st2 = bwd_skip(t, lse, g, bm, 1e-5, w.M, w.V, w.d, 30.0, dW_init=init, accumulate=True)
+    dh3, _, st3 = bwd_skip(t, lse, g, bm, 1e-5, w.M, w.V, w.d, 30.0, with_dW=False)
+    assert st == st2 == st3 == 0
+    assert np.array_equal(dh, dh2) and np.array_equal(dh, dh3)
+    np.testing.assert_allclose(dW2, init + dW, rtol=1e-6, atol=1e-6)
+
+
+def test_multiblock_skip_on_sampled_tiles():
+    # 2 row blocks x 8 vocabulary blocks (blocks of 16384 x 8192); sampled row tiles and vocabulary
+    # tiles against the oracle, whose filter tiles line up with the library's
+    w = workloads.make("e4b_sharp", M=16384 + 512, d=256, V=65536)   # about half the tiles dropped
+    assert w.M == 16896
+    t = to_dev(w)
+    _, lse, bm, st = fwd_bmax(t, w.M, w.V, w.d, 30.0)
+    assert st == 0
+    rng = np.random.default_rng(4)
+    g = (rng.standard_normal(w.M) * 1e-3 * (w.mask != 0)).astype(np.float32)
+    eps = 1e-5
+    dh, dW, st = bwd_skip(t, lse, g, bm, eps, w.M, w.V, w.d, 30.0)
+    assert st == 0
+    dh1, dW1, st1 = bwd_skip(t, lse, g, None, eps, w.M, w.V, w.d, 30.0)
+    assert st1 == 0 and np.array_equal(dh, dh1) and np.array_equal(dW, dW1)
+    h, W = f64(w.h), f64(w.W)
+    for mt in (0, 127, 128, w.M // 128 - 1):          # first / last tile of each row block
+        r = slice(128 * mt, min(w.M, 128 * mt + 128))
+        rdh, _ = oracle.head_backward(h[r], W, w.targets[r], w.mask[r], lse[r], g[r], 30.0, filter_eps=eps)
+        assert relfro(dh[r], rdh) < GRAD_RELFRO
+    for vt in (0, 31, 32, 255):                       # across vocabulary blocks, the last one included
+        c0 = 256 * vt
+        _, rdW = oracle.head_backward(h, W, w.targets, w.mask, lse, g, 30.0, filter_eps=eps, vocab=(c0, c0 + 256))
+        if np.linalg.norm(rdW) == 0:
+            assert not dW[c0:c0 + 256].any()
+        else:
+            assert relfro(dW[c0:c0 + 256], rdW) < GRAD_RELFRO

@@ -140,3 +140,20 @@ def test_block_max_bounds_the_softmax():
     bound = np.exp2(bm[q][:, j] - lse[:, None] / math.log(2))
     rows = w.mask != 0
     assert np.all(p[rows] <= bound[rows] * (1 + 1e-12))
+
+
+@pytest.mark.parametrize("eps", [0.0, 3e-3])
+def test_vocab_slices_reassemble_the_whole(eps):
+    # dW is separable over vocabulary rows and dh over columns: the slices add up to the whole
+    w = workloads.make("tiny", M=70, d=32, V=600)
+    h, W = oracle.bf16_bits_to_f64(w.h), oracle.bf16_bits_to_f64(w.W)
+    g = np.random.default_rng(7).standard_normal(w.M) * w.mask
+    lse = oracle.head_forward(h, W, w.targets, w.mask, 30.0)[1]
+    tile = (8, 32)
+    dh, dW = oracle.head_backward(h, W, w.targets, w.mask, lse, g, 30.0, filter_eps=eps, tile=tile)
+    parts = [oracle.head_backward(h, W, w.targets, w.mask, lse, g, 30.0, filter_eps=eps, tile=tile, vocab=(c, min(600, c + 256)))
+             for c in range(0, 600, 256)]
+    np.testing.assert_allclose(sum(p[0] for p in parts), dh, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(np.concatenate([p[1] for p in parts]), dW, rtol=1e-12, atol=1e-15)
+    with pytest.raises(oracle.OracleError):
+        oracle.head_backward(h, W, w.targets, w.mask, lse, g, 30.0, tile=tile, vocab=(16, 64))

@@ -25,6 +25,12 @@ and MiniCPM5, is not available, and these synthetic draws stand in for it):
   ragged   64 pairs, 128 lengths ~ U{16..1024} packed, then pad rows
            (mask 0, seq_id -1) up to a multiple of 128; d 3840, V 262144;
            softcap 30; rows t < M/2 peaked as in e4b, the rest N(0,1); lambda 0.1.
+  e4b_sharp  e4b's shapes and targets with a sharper peak, h_t = 0.5 N(0,1) +
+           12 W[y_t] / |W[y_t]|: the target logit is about 24 (19.9 after the
+           softcap) against N(0, 1.2) elsewhere, so p(target) ~ 0.999.  It
+           stands in for the pages' real teacher-forced data, on which the
+           backward skips were measured; e4b's own peak (3) leaves the softmax
+           nearly flat at V = 262144 (p(target) ~ 1e-3).
 """
 
 from __future__ import annotations
@@ -113,13 +119,13 @@ def normal_bf16(seed: int, key: int, shape, std: float) -> np.ndarray:
 
 
 def _peaked_h(seed: int, W_bits: np.ndarray, targets: np.ndarray, rows: np.ndarray, d: int,
-              key: int = K_H) -> np.ndarray:
-    """bf16 bits of 0.5 N(0,1) + 3 W[y] / |W[y]| for the given rows (input recipe only)."""
+              key: int = K_H, peak: float = 3.0) -> np.ndarray:
+    """bf16 bits of 0.5 N(0,1) + peak W[y] / |W[y]| for the given rows (input recipe only)."""
     noise = bf16_to_f32(normal_bf16(seed, key, (len(rows), d), 1.0)).astype(np.float64)
     Wy = bf16_to_f32(W_bits[targets[rows]]).astype(np.float64)
     nrm = np.linalg.norm(Wy, axis=1, keepdims=True)
     nrm[nrm == 0] = 1.0
-    return round_bf16((0.5 * noise + 3.0 * Wy / nrm).astype(np.float32))
+    return round_bf16((0.5 * noise + peak * Wy / nrm).astype(np.float32))
 
 
 def _layout(lengths: np.ndarray, prompt_rows: int = 0, pad_to: int = 1):
@@ -148,7 +154,7 @@ def _zipf_targets(seed, M, V, a=1.1):
     return np.minimum(np.searchsorted(cdf, u, side="right"), V - 1).astype(np.int32)
 
 
-NAMES = ("tiny", "small", "e4b", "largev", "ragged")
+NAMES = ("tiny", "small", "e4b", "largev", "ragged", "e4b_sharp")
 
 
 def make(name: str, seed: int = 0, M: int | None = None, d: int | None = None,
@@ -179,7 +185,7 @@ def make(name: str, seed: int = 0, M: int | None = None, d: int | None = None,
         W = normal_bf16(seed, K_W, (V, d), (4.0 / d) ** 0.5)
         h = normal_bf16(seed, K_H, (Mx, d), 1.0)
         return Workload(name, h, W, tg, mask, seq_id, P, 0.0, 0.1)
-    if name == "e4b":
+    if name in ("e4b", "e4b_sharp"):
         d = d or 2560
         V = V or 262144
         L = 256
@@ -189,7 +195,7 @@ def make(name: str, seed: int = 0, M: int | None = None, d: int | None = None,
         Mx = len(seq_id)
         tg = _uniform_targets(seed, Mx, V)
         W = normal_bf16(seed, K_W, (V, d), (4.0 / d) ** 0.5)
-        h = _peaked_h(seed, W, tg, np.arange(Mx), d)
+        h = _peaked_h(seed, W, tg, np.arange(Mx), d, peak=3.0 if name == "e4b" else 12.0)
         return Workload(name, h, W, tg, mask, seq_id, P, 30.0, 0.1)
     if name == "largev":
         d = d or 4096
