@@ -329,7 +329,7 @@ def head_block_max(h: np.ndarray, W: np.ndarray, mask: np.ndarray, softcap: floa
 
 def head_backward(h: np.ndarray, W: np.ndarray, targets: np.ndarray, mask: np.ndarray,
                   lse: np.ndarray, g: np.ndarray, softcap: float = 0.0, filter_eps: float = 0.0,
-                  tile=(TILE_ROWS, TILE_COLS)):
+                  tile=(TILE_ROWS, TILE_COLS), vocab=None):
     """dh = dZ W and dW = dZ^T h with dZ = g (onehot_y - softmax(z~)) sech^2(z/c).
 
     softmax is rebuilt from the given lse: p = exp(z~ - lse).  Rows with
@@ -337,14 +337,26 @@ def head_backward(h: np.ndarray, W: np.ndarray, targets: np.ndarray, mask: np.nd
     read).  With ``filter_eps`` > 0 the coefficient filter of the backward
     skips applies: every ``tile`` of dZ whose coefficient entries all lie below
     filter_eps is dropped (see ``_tile_keep``).  Returns (dh [M, d], dW [V, d])
-    in float64.
+    in float64.  ``vocab = (c0, c1)`` restricts the sums to vocabulary columns
+    [c0, c1) (c0 on a tile boundary; lse still covers the whole vocabulary):
+    dh is then their share of the gradient and dW holds rows c0 .. c1-1 only.
     """
     h = np.asarray(h, dtype=np.float64)
     W = np.asarray(W, dtype=np.float64)
     M, d = h.shape
-    V = W.shape[0]
     targets = np.asarray(targets).astype(np.int64)
     mask = np.asarray(mask).astype(bool)
+    if vocab is not None:
+        c0, c1 = vocab
+        if c0 % tile[1] != 0:
+            raise OracleError("arg", "a vocabulary slice starts on a tile boundary")
+        W = W[c0:c1]
+        inside = (targets >= c0) & (targets < c1)
+        targets = np.where(inside, targets - c0, 0)
+        onehot_rows = mask & inside
+    else:
+        onehot_rows = mask
+    V = W.shape[0]
     lse = np.asarray(lse, dtype=np.float64)
     g = np.where(mask, np.asarray(g, dtype=np.float64), 0.0)
     dh = np.zeros((M, d))
@@ -362,7 +374,7 @@ def head_backward(h: np.ndarray, W: np.ndarray, targets: np.ndarray, mask: np.nd
         p = np.exp(zt - lse[r0:r1, None])
         onehot = np.zeros_like(p)
         rows = np.arange(r1 - r0)
-        m = mask[r0:r1]
+        m = onehot_rows[r0:r1]
         onehot[rows[m], targets[r0:r1][m]] = 1.0
         coef = (onehot - p) * softcap_slope(z, softcap)
         if filter_eps > 0:
