@@ -120,10 +120,20 @@ size_t wblock_bytes(int64_t M, int64_t V, int64_t d) { return (size_t)wblock_row
 constexpr int kCounters = 4096;
 constexpr size_t kCounterBytes = kCounters * sizeof(int);
 
-// Backward-skip area after the counters: tile list + count, dh / dW k-lists and counts (ints), then
-// the filter's keep flags (bytes).
-constexpr size_t kSkipBytes = 96 << 10;
-static_assert((size_t)kMaxTiles * (5 * sizeof(int) + 1) + 64 <= kSkipBytes, "skip area too small");
+// Backward-skip area after the counters: one slot per (row block, vocabulary block) of a plan round
+// (tile list, count and keep bitmaps; SkipShape).  A slot is at most ~34 KiB, so a round covers
+// 120 or more blocks.
+constexpr size_t kSkipBytes = 4 << 20;
+
+SkipShape skip_shape(const BwdBlocks& b) {
+  SkipShape s{};
+  s.n_mt = (int)(b.Mc / kBM);
+  s.n_vt = (int)(b.Vc / kBN);
+  s.ld_row = (s.n_vt + 31) / 32;
+  s.ld_col = (s.n_mt + 31) / 32;
+  s.slot_bytes = (s.end() + 255) & ~size_t(255);
+  return s;
+}
 
 // Number of vocabulary splits: minimise (waves of units) x (tiles per unit);
 // ties go to fewer splits (fewer partials to merge).
@@ -308,22 +318,21 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   const BwdBlocks B = bwd_blocks(M, V);
   void* S = align_ws(workspace);
   int* counters = reinterpret_cast<int*>(static_cast<uint8_t*>(S) + scratch_bytes(M, V));
-  // backward skips: plan / index lists in the area after the counters
+  // backward skips: plan rounds over the blocks, slots in the area after the counters
   const bool skip = eps > 0.f;
   SkipPlan P{};
-  {
-    int* a = counters + kCounters;
-    P.list = a;
-    P.count = a + kMaxTiles;
-    P.rowlist = a + kMaxTiles + 16;
-    P.rowcnt = P.rowlist + kMaxTiles;
-    P.collist = P.rowcnt + kMaxTiles;
-    P.colcnt = P.collist + kMaxTiles;
-    P.flags = reinterpret_cast<uint8_t*>(P.colcnt + kMaxTiles);
+  const int64_t n_mblocks = cdiv(M, B.Mc), nblocks_all = n_mblocks * cdiv(V, B.Vc);
+  int round_slots = 1;
+  if (skip) {
     P.g = g, P.mask = mask, P.targets = targets, P.lse = lse, P.bmax = bmax;
     P.bmax_ld = (int)cdiv(V, kBN);
     P.M = (int)M, P.V = (int)V, P.status = status;
-    P.thr2 = skip ? log2f(eps) : 0.f;
+    P.Mc = B.Mc, P.Vc = B.Vc, P.n_mblocks = (int)n_mblocks;
+    P.shape = skip_shape(B);
+    P.area = reinterpret_cast<uint8_t*>(counters + kCounters);
+    P.thr2 = log2f(eps);
+    if ((int64_t)P.shape.n_mt * P.shape.n_vt > kMaxTiles) return ORPO_ERR_SHAPE;  // cannot happen: Mc Vc bounded
+    round_slots = (int)std::min<int64_t>(nblocks_all, (int64_t)(kSkipBytes / P.shape.slot_bytes));
   }
   void* Wb = q ? wblock_ptr(workspace, M, V) : nullptr;
   int64_t launch = 0;
@@ -361,6 +370,7 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   R.kblocks = (int)cdiv(d, 64);
   const int n_nt = (int)cdiv(d, kBN);
 
+  int64_t block = 0;  // v-block major, m-block minor
   for (int64_t v0 = 0, vblock = 0; v0 < V; v0 += B.Vc, ++vblock) {
     const int64_t vc = std::min(B.Vc, V - v0);
     if (q) {
@@ -378,21 +388,26 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
       R.n_mt = n_mt;
       R.n_vt = n_vt;
       R.grid = (int)std::min<int64_t>((int64_t)n_mt * n_vt, sms);
+      uint32_t *rowbits = nullptr, *colbits = nullptr;
       if (skip) {
-        if ((int64_t)n_mt * n_vt > kMaxTiles) return ORPO_ERR_SHAPE;  // cannot happen: Mc * Vc is bounded
-        P.m0 = (int)m0, P.mc = (int)mc, P.v0 = (int)v0, P.vc = (int)vc, P.n_mt = n_mt, P.n_vt = n_vt;
-        if (bmax) {  // block skip: plan the tiles to recompute (and zero the flags)
+        const int64_t slot = block % round_slots;
+        if (slot == 0) {  // plan the next round of blocks (zeroed bitmaps; tile lists with block maxima)
+          P.first_block = (int)block;
+          P.nblocks = (int)std::min<int64_t>(round_slots, nblocks_all - block);
           if (launch_skip_plan(P, st) != cudaSuccess) return ORPO_ERR_CUDA;
-          R.list = P.list;
-          R.count = P.count;
-        } else if (cudaMemsetAsync(P.flags, 0, (size_t)n_mt * n_vt, st) != cudaSuccess) {
-          return ORPO_ERR_CUDA;
         }
-        R.flags = P.flags;
+        uint8_t* base = P.area + (size_t)slot * P.shape.slot_bytes;
+        rowbits = reinterpret_cast<uint32_t*>(base + P.shape.rowbits_off());
+        colbits = reinterpret_cast<uint32_t*>(base + P.shape.colbits_off());
+        if (bmax) {
+          R.list = reinterpret_cast<const int*>(base + P.shape.list_off());
+          R.count = reinterpret_cast<const int*>(base + P.shape.count_off());
+        }
+        R.rowbits = rowbits, R.colbits = colbits, R.ld_row = P.shape.ld_row, R.ld_col = P.shape.ld_col;
         R.eps = eps;
       }
+      ++block;
       if (launch_recompute(R, st) != cudaSuccess) return ORPO_ERR_CUDA;
-      if (skip && launch_skip_index(P, st) != cudaSuccess) return ORPO_ERR_CUDA;
 
       GemmClassH cdw{};  // dW[v0 + ..] (+)= S^T h[m0 + ..]
       if (dW) {
@@ -404,7 +419,8 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
         cdw.n_mt = (int)cdiv(vc, kBM), cdw.n_nt = n_nt, cdw.kblocks = (int)cdiv(mc, 64);
         cdw.mt_major = 1;  // CTAs running together share one column slab of S; h stays in L2
         if (skip) {        // K: the kept row tiles of this 128-column tile's vocabulary tile, 2 k-blocks each
-          cdw.klist = P.collist, cdw.kcnt = P.colcnt, cdw.list_ld = n_mt, cdw.list_shift = 1, cdw.kg_shift = 1;
+          cdw.kbits = colbits, cdw.kwords = P.shape.ld_col, cdw.list_shift = 1, cdw.kg_shift = 1;
+          cdw.ngroups = n_mt, cdw.clip = n_mt * 2 - cdw.kblocks;
         }
       }
       GemmClassH cdh{};  // dh[m0 + ..] (+)= S W[v0 + ..]
@@ -416,7 +432,8 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
       cdh.n_mt = n_mt, cdh.n_nt = n_nt, cdh.kblocks = (int)cdiv(vc, 64);
       cdh.mt_major = 1;
       if (skip) {  // K: the kept vocabulary tiles of this row tile, 4 k-blocks each
-        cdh.klist = P.rowlist, cdh.kcnt = P.rowcnt, cdh.list_ld = n_vt, cdh.list_shift = 0, cdh.kg_shift = 2;
+        cdh.kbits = rowbits, cdh.kwords = P.shape.ld_row, cdh.list_shift = 0, cdh.kg_shift = 2;
+        cdh.ngroups = n_vt, cdh.clip = n_vt * 4 - cdh.kblocks;
       }
       // longer tiles first
       if (dW && cdw.kblocks >= cdh.kblocks) {

@@ -119,22 +119,47 @@ struct Operand {
   int k0;        // first K coordinate of k-block 0
 };
 
-// kblocks k-blocks of BK, in order.  Dense (klist == nullptr): k-block i is i.  Sparse: k-block i is
-// (klist[i >> kg_shift] << kg_shift) + (i & ((1 << kg_shift) - 1)), i.e. the list names groups of
-// 2^kg_shift consecutive k-blocks (ascending; only the last group may be cut short by kblocks).  A tile
-// with kblocks == 0 issues no loads and no MMAs and takes no accumulator; the kernel's epilogue
-// handles it without waiting on the accumulator.
+// kblocks k-blocks of BK, in order.  Dense (kbits == nullptr): k-block i is i.  Sparse: kbits is a
+// bitmap (kwords 32-bit words) of groups of 2^kg_shift consecutive k-blocks; the tile walks the set
+// groups in ascending order, and kblocks (the count of set groups x 2^kg_shift, less what lies past
+// the operands' K extent in the last group) ends the walk.  A tile with kblocks == 0 issues no loads
+// and no MMAs and takes no accumulator; the kernel's epilogue handles it without waiting on one.
 struct TileOps {
   Operand a, b;
   int kblocks;
-  const int* klist = nullptr;
+  const uint32_t* kbits = nullptr;
+  int kwords = 0;
   int kg_shift = 0;
 };
 
-__device__ __forceinline__ int tile_kblock(const TileOps& t, int i) {
-  if (t.klist == nullptr) return i;
-  return (__ldg(t.klist + (i >> t.kg_shift)) << t.kg_shift) + (i & ((1 << t.kg_shift) - 1));
-}
+// Walks the k-blocks of a tile; a sparse bitmap is read one word ahead, so the TMA issue of a group
+// seldom waits on the load of its own word.
+struct KWalk {
+  const uint32_t* bits;
+  int words, shift, w, group;
+  uint32_t cur, nxt;
+  __device__ __forceinline__ explicit KWalk(const TileOps& t)
+      : bits(t.kbits), words(t.kwords), shift(t.kg_shift), w(0), group(0), cur(0), nxt(0) {
+    if (bits != nullptr && words > 0) {
+      cur = __ldg(bits);
+      nxt = words > 1 ? __ldg(bits + 1) : 0u;
+    }
+  }
+  __device__ __forceinline__ int kblock(int i) {
+    if (bits == nullptr) return i;
+    const int off = i & ((1 << shift) - 1);
+    if (off == 0) {
+      while (cur == 0u && w + 1 < words) {  // next word with a set group (bounded by the bitmap)
+        ++w;
+        cur = nxt;
+        nxt = w + 1 < words ? __ldg(bits + w + 1) : 0u;
+      }
+      group = 32 * w + __ffs((int)cur) - 1;
+      cur &= cur - 1u;
+    }
+    return (group << shift) + off;
+  }
+};
 
 __device__ __forceinline__ uint8_t* smem_base_aligned() {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -208,8 +233,9 @@ __device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* sme
     const int len = sched.unit_len(u);
     for (int j = 0; ok && j < len; ++j) {
       const TileOps t = sched.tile(u, j);
+      KWalk walk(t);
       for (int i = 0; i < t.kblocks; ++i, ++it) {
-        const int kb = tile_kblock(t, i);
+        const int kb = walk.kblock(i);
         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
         if (!wait_phase(ctl, &ctl->empty[s], ph ^ 1u, status)) {
           ok = false;

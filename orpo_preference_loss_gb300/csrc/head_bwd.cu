@@ -50,8 +50,10 @@ struct RecArgs {
   int M, V;
   float softcap;
   int32_t* status;
-  float eps;       // coefficient filter threshold (filter instances only)
-  uint8_t* flags;  // [n_mt][n_vt] of the block: set to 1 for a tile the filter keeps (filter instances only)
+  float eps;           // coefficient filter threshold (filter instances only)
+  uint32_t* rowbits;   // filter instances: kept tiles by row tile, [n_mt][ld_row] bitmap over vt
+  uint32_t* colbits;   //                   and by vocabulary tile, [n_vt][ld_col] bitmap over mt
+  int ld_row, ld_col;
 };
 
 // dZ for 32 accumulator values of one row starting at vocabulary column col0;
@@ -132,8 +134,8 @@ __device__ __forceinline__ void dz_chunk(const uint32_t (&r)[32], int col0, int 
 }
 
 // kFilter: the coefficient filter of the backward skips ("Steel flash-CCE — handoff" §E).  A tile
-// is kept (flags = 1) when some row with g != 0 has |dZ| >= eps |g|, i.e. an entry of
-// (onehot - p) sech^2 reaches eps; the dh / dW GEMMs read only kept tiles.
+// is kept (its bits set in rowbits and colbits) when some row with g != 0 has |dZ| >= eps |g|,
+// i.e. an entry of (onehot - p) sech^2 reaches eps; the dh / dW GEMMs read only kept tiles.
 template <int cap, bool kFilter>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     rec_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mw,
@@ -207,7 +209,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       epi_release(ctl, tcount);
       if constexpr (kFilter) {
         const bool keep = gval != 0.f && amax >= p.eps * fabsf(gval);
-        if (__any_sync(0xffffffffu, keep) && lane == 0) p.flags[mt * sched.n_vt + vt] = 1;
+        if (__any_sync(0xffffffffu, keep) && lane == 0) {
+          atomicOr(p.rowbits + mt * p.ld_row + (vt >> 5), 1u << (vt & 31));
+          atomicOr(p.colbits + vt * p.ld_col + (mt >> 5), 1u << (mt & 31));
+        }
       }
     }
     if (lane == 0) bulk_wait_group<0>();
@@ -223,11 +228,11 @@ struct GemmClass {
   int out_rows, out_cols;
   int n_mt, n_nt, kblocks;
   int mt_major;
-  // sparse K (backward skips): list (mt >> list_shift) of k-block groups, list_ld entries apart, with
-  // its k-block count in kcnt; groups are 2^kg_shift k-blocks.  klist == nullptr: dense, kblocks.
-  const int* klist;
-  const int* kcnt;
-  int list_ld, list_shift, kg_shift;
+  // sparse K (backward skips): bitmap (mt >> list_shift) of kept groups of 2^kg_shift k-blocks,
+  // kwords words each; ngroups groups in all, the last holding clip k-blocks fewer than the others
+  // (past the operands' K extent).  kbits == nullptr: dense, kblocks.
+  const uint32_t* kbits;
+  int kwords, list_shift, kg_shift, ngroups, clip;
 };
 
 struct GemmSched {
@@ -276,11 +281,16 @@ struct GemmSched {
     t.a = Operand{map(c.a_map), c.a_mn, c.a_mn_base + mt * BM, c.a_k_base};
     t.b = Operand{map(c.b_map), c.b_mn, c.b_mn_base + nt * BN, c.b_k_base};
     t.kblocks = c.kblocks;
-    if (c.klist != nullptr) {
-      const int li = mt >> c.list_shift;
-      t.klist = c.klist + (size_t)li * c.list_ld;
-      t.kblocks = __ldg(c.kcnt + li);
+    if (c.kbits != nullptr) {
+      const uint32_t* bits = c.kbits + (size_t)(mt >> c.list_shift) * c.kwords;
+      int n = 0;
+      for (int w = 0; w < c.kwords; ++w) n += __popc(__ldg(bits + w));
+      const int lg = c.ngroups - 1;
+      const bool last = (__ldg(bits + (lg >> 5)) >> (lg & 31)) & 1u;
+      t.kbits = bits;
+      t.kwords = c.kwords;
       t.kg_shift = c.kg_shift;
+      t.kblocks = (n << c.kg_shift) - (last ? c.clip : 0);
     }
     return t;
   }
@@ -393,7 +403,8 @@ cudaError_t launch_rec_kernel(const RecLaunch& L, cudaStream_t st) {
   static int smem_set[64] = {0};
   if (cudaError_t e = opt_in_smem(rec_kernel<cap, kFilter>, SMEM_TOTAL, smem_set)) return e;
   RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks, L.w_row0, L.list, L.count};
-  RecArgs a{L.targets, L.mask, L.lse, L.g, L.M, L.V, L.softcap, L.status, L.eps, L.flags};
+  RecArgs a{L.targets, L.mask, L.lse, L.g, L.M, L.V, L.softcap, L.status, L.eps, L.rowbits, L.colbits, L.ld_row,
+            L.ld_col};
   prof_begin(K_REC, st);
   rec_kernel<cap, kFilter><<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, L.ms_store, sched, a);
   prof_end(K_REC, st);
@@ -410,7 +421,7 @@ cudaError_t launch_rec_cap(const RecLaunch& L, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st) {
-  return L.flags ? launch_rec_cap<true>(L, st) : launch_rec_cap<false>(L, st);
+  return L.rowbits ? launch_rec_cap<true>(L, st) : launch_rec_cap<false>(L, st);
 }
 
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
@@ -423,7 +434,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
     sched.cls[k] = GemmClass{h.a_map,     h.a_mn,      h.a_mn_base,  h.a_k_base,     h.b_map,        h.b_mn,
                              h.b_mn_base, h.b_k_base,  h.out_map,    h.out_row_base, h.out_col_base, h.reduce,
                              h.out_rows,  h.out_cols,  h.n_mt,       h.n_nt,         h.kblocks,      h.mt_major,
-                             h.klist,     h.kcnt,      h.list_ld,    h.list_shift,   h.kg_shift};
+                             h.kbits,     h.kwords,    h.list_shift, h.kg_shift,     h.ngroups,      h.clip};
   }
   prof_begin(kind, st);
   gemm_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.maps[0], L.maps[1], L.maps[2], L.maps[3], L.maps[4],

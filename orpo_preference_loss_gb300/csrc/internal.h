@@ -72,32 +72,44 @@ struct RecLaunch {
   // backward skips
   const int* list = nullptr;   // tiles to compute (vt * n_mt + mt, ascending) and their count, or all tiles
   const int* count = nullptr;
-  uint8_t* flags = nullptr;    // coefficient filter: [n_mt][n_vt] keep flags (zeroed), or nullptr for no filter
+  uint32_t* rowbits = nullptr;  // coefficient filter: zeroed keep bitmaps [n_mt][ld_row] and [n_vt][ld_col],
+  uint32_t* colbits = nullptr;  // or nullptr for no filter
+  int ld_row = 0, ld_col = 0;
   float eps = 0.f;
 };
 cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st);
 
 // ---- backward skips (skip.cu): per (row block, vocabulary block), tiles of 128 x 256
+// One plan launch covers a round of consecutive blocks (v-block major, m-block minor, as the backward
+// walks them), one CTA per block, each with its own slot in the skip area:
+//   ints  list[n_mt * n_vt]  tiles to recompute (vt * n_mt + mt, ascending), then count
+//   words rowbits[n_mt][ld_row], colbits[n_vt][ld_col]  the filter's keep bitmaps (zeroed by the plan)
+struct SkipShape {
+  int n_mt, n_vt, ld_row, ld_col;
+  size_t slot_bytes;
+  __host__ __device__ size_t list_off() const { return 0; }
+  __host__ __device__ size_t count_off() const { return (size_t)n_mt * n_vt * 4; }
+  __host__ __device__ size_t rowbits_off() const { return count_off() + 16; }
+  __host__ __device__ size_t colbits_off() const { return rowbits_off() + (size_t)n_mt * ld_row * 4; }
+  __host__ __device__ size_t end() const { return colbits_off() + (size_t)n_vt * ld_col * 4; }
+};
 struct SkipPlan {
   const float* g;
   const uint8_t* mask;
   const int32_t* targets;
   const float* lse;
-  const float* bmax;  // forward block maxima [ceil(M/32)][bmax_ld], base 2; nullptr: no block skip
+  const float* bmax;  // forward block maxima [ceil(M/32)][bmax_ld], base 2; nullptr: filter only (no lists)
   int bmax_ld;
-  int m0, mc, v0, vc, n_mt, n_vt, M, V;
+  int M, V;
+  int64_t Mc, Vc;     // block sizes; blocks are numbered b = vblock * n_mblocks + mblock
+  int n_mblocks;
+  int first_block, nblocks;  // this round: blocks first_block .. first_block + nblocks - 1, slot b - first_block
+  SkipShape shape;    // of a full block (edge blocks use a prefix of it)
+  uint8_t* area;      // slot s at area + s * shape.slot_bytes
   float thr2;         // log2(eps)
-  int* list;          // [kMaxTiles] tiles to recompute (vt * n_mt + mt, ascending) and their count
-  int* count;
-  uint8_t* flags;     // [n_mt][n_vt] keep flags of the coefficient filter
   int32_t* status;
-  int* rowlist;       // [n_mt][n_vt] kept vocabulary tiles per row tile (dh GEMM), rowcnt[n_mt] k-blocks
-  int* rowcnt;
-  int* collist;       // [n_vt][n_mt] kept row tiles per vocabulary tile (dW GEMM), colcnt[n_vt] k-blocks
-  int* colcnt;
 };
-cudaError_t launch_skip_plan(const SkipPlan& P, cudaStream_t st);   // zeroes flags; lists the tiles to recompute
-cudaError_t launch_skip_index(const SkipPlan& P, cudaStream_t st);  // GEMM k-lists from the filter's flags
+cudaError_t launch_skip_plan(const SkipPlan& P, cudaStream_t st);  // lists and zeroed bitmaps for a round
 
 // ---- quantised head: affine group dequantisation of W rows [v0, v0 + rows) into bf16 [rows, d]
 cudaError_t launch_dequant(const uint8_t* wq, const void* scales, const void* biases, int bits, int group,
@@ -111,11 +123,10 @@ struct GemmClassH {
   int out_rows, out_cols;  // valid extent of the output tensor
   int n_mt, n_nt, kblocks;
   int mt_major;
-  // sparse K (backward skips): per list index (mt >> list_shift), ascending groups of 2^kg_shift
-  // k-blocks at klist + index * list_ld and their k-block count kcnt[index]; nullptr: dense
-  const int* klist = nullptr;
-  const int* kcnt = nullptr;
-  int list_ld = 0, list_shift = 0, kg_shift = 0;
+  // sparse K (backward skips): bitmap (mt >> list_shift) of kept groups of 2^kg_shift k-blocks at
+  // kbits + index * kwords; ngroups groups, the last clip k-blocks short; nullptr: dense
+  const uint32_t* kbits = nullptr;
+  int kwords = 0, list_shift = 0, kg_shift = 0, ngroups = 0, clip = 0;
 };
 struct GemmLaunch {
   CUtensorMap maps[6];

@@ -5,21 +5,18 @@
 // backward coefficient that lies wholly below eps, and the block skip uses the
 // forward's block maxima to skip cold (token block, vocabulary block) work.
 //
-// Here a block is one 128 x 256 tile of dZ.  Per (row block, vocabulary block)
-// of the backward:
-//   plan_kernel  : before the recompute.  A tile holds work unless it is
-//                  provably cold: no row with g != 0 has its target in the
-//                  tile, and for every 32-row group, (largest logit of the group
-//                  in the tile) - (smallest lse of the group's rows with g != 0)
-//                  lies below log2(eps) - kMargin in base-2 units, which bounds
-//                  every p sech^2 of the tile below eps.  The remaining tiles
-//                  are listed (vocabulary-tile-major, ascending) for the
-//                  recompute; the filter would drop every cold tile anyway, so
-//                  the block skip leaves the result unchanged.
-//   index_kernel : after the recompute, whose filter marked the kept tiles.
-//                  Builds, per row tile, the ascending list of kept vocabulary
-//                  tiles (K of the dh GEMM) and, per vocabulary tile, the list
-//                  of kept row tiles (K of the dW GEMM), with k-block counts.
+// Here a block is one 128 x 256 tile of dZ.  One plan launch serves a round of
+// (row block, vocabulary block) pairs of the backward, one CTA per pair, before
+// their recomputes.  Each CTA zeroes its pair's keep bitmaps (the recompute's
+// filter sets the bits of the tiles it keeps; the dh / dW GEMMs walk them) and,
+// when the forward's block maxima are given, lists the tiles to recompute.  A
+// tile holds work unless it is provably cold: no row with g != 0 has its target
+// in the tile, and for every 32-row group, (largest logit of the group in the
+// tile) - (smallest lse of the group's rows with g != 0) lies below
+// log2(eps) - kMargin in base-2 units, which bounds every p sech^2 of the tile
+// below eps.  The filter would drop every cold tile anyway, so the block skip
+// leaves the result unchanged.  The list is vocabulary-tile-major and
+// ascending, the order of the full recompute.
 #include "internal.h"
 
 #include <cuda_runtime.h>
@@ -36,38 +33,45 @@ constexpr int kPlanThreads = 1024;
 constexpr int kGroupsMax = kMcMax / 32;
 static_assert(kMaxTiles == 4 * kPlanThreads, "the plan judges four tiles per thread");
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const float* __restrict__ g, const uint8_t* __restrict__ mask,
-                                                            const int32_t* __restrict__ targets,
-                                                            const float* __restrict__ lse,
-                                                            const float* __restrict__ bmax, int bmax_ld, int m0, int mc,
-                                                            int v0, int vc, int n_mt, int n_vt, int M, int V,
-                                                            float thr2, int* __restrict__ list, int* __restrict__ count,
-                                                            uint8_t* __restrict__ flags, int32_t* status) {
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const SkipPlan P) {
   __shared__ uint8_t hot[kMaxTiles];        // [mt][vt]: a target of an active row lies in the tile
   __shared__ float minlse2[kGroupsMax];     // per 32-row group: min lse log2e over active rows (+inf: none)
   __shared__ int warp_sums[kPlanThreads / 32];
   const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int b = P.first_block + (int)blockIdx.x;
+  const int mb = b % P.n_mblocks, vb = b / P.n_mblocks;
+  const int m0 = (int)(mb * P.Mc), v0 = (int)(vb * P.Vc);
+  const int mc = (int)min((int64_t)P.M - m0, P.Mc), vc = (int)min((int64_t)P.V - v0, P.Vc);
+  const int n_mt = (mc + 127) / 128, n_vt = (vc + 255) / 256;
+  uint8_t* slot = P.area + (size_t)blockIdx.x * P.shape.slot_bytes;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(slot + P.shape.rowbits_off());  // rowbits, then colbits
+  const int nwords = P.shape.n_mt * P.shape.ld_row + P.shape.n_vt * P.shape.ld_col;
+  for (int i = tid; i < nwords; i += kPlanThreads) bits[i] = 0u;
+  if (P.bmax == nullptr) return;  // filter alone: every tile is recomputed
+
+  int* list = reinterpret_cast<int*>(slot + P.shape.list_off());
+  int* count = reinterpret_cast<int*>(slot + P.shape.count_off());
   const int ntiles = n_mt * n_vt;
   const int ngroups = (mc + 31) / 32;
-  for (int i = tid; i < ntiles; i += kPlanThreads) {
-    hot[i] = 0;
-    flags[i] = 0;
-  }
+  for (int i = tid; i < ntiles; i += kPlanThreads) hot[i] = 0;
   __syncthreads();
-  for (int qg = tid; qg < ngroups; qg += kPlanThreads) {
-    float mn = INFINITY;
-    for (int r = qg * 32; r < min(mc, qg * 32 + 32); ++r) {
-      const int t = m0 + r;
-      if (t >= M || mask[t] == 0 || g[t] == 0.f) continue;
-      mn = fminf(mn, lse[t] * kLog2e);
-      const int y = targets[t];
-      if (y < 0 || y >= V) {
-        atomicOr(status, ORPO_STATUS_TARGET);
-        continue;
-      }
-      if (y >= v0 && y < v0 + vc) hot[(r / 128) * n_vt + (y - v0) / 256] = 1;
+  // one row per thread: a warp covers one 32-row group per pass
+  for (int r = tid; r < ngroups * 32; r += kPlanThreads) {
+    const int t = m0 + r;
+    const bool active = r < mc && t < P.M && P.mask[t] != 0 && P.g[t] != 0.f;
+    float l2 = INFINITY;
+    if (active) {
+      l2 = P.lse[t] * kLog2e;
+      const int y = P.targets[t];
+      if (y < 0 || y >= P.V)
+        atomicOr(P.status, ORPO_STATUS_TARGET);
+      else if (y >= v0 && y < v0 + vc)
+        hot[(r / 128) * n_vt + (y - v0) / 256] = 1;
     }
-    minlse2[qg] = mn;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l2 = fminf(l2, __shfl_xor_sync(0xffffffffu, l2, o));
+    if (lane == 0) minlse2[r / 32] = l2;
   }
   __syncthreads();
   // each thread judges 4 consecutive tiles in list order (u = vt * n_mt + mt), then a block scan
@@ -83,14 +87,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const float* __restr
     for (int gq = mt * 4; !hit && gq < min(ngroups, mt * 4 + 4); ++gq) {
       const float ml = minlse2[gq];
       if (ml == INFINITY) continue;
-      const float bm = __ldg(bmax + (size_t)(m0 / 32 + gq) * bmax_ld + (v0 / 256 + vt));
-      hit = bm - ml >= thr2 - kMargin;  // -inf block maxima (no supervised row) never hold work
+      const float bm = __ldg(P.bmax + (size_t)(m0 / 32 + gq) * P.bmax_ld + (v0 / 256 + vt));
+      hit = bm - ml >= P.thr2 - kMargin;  // -inf block maxima (no supervised row) never hold work
     }
     keep[k] = hit;
     c += hit;
   }
   // exclusive scan of c over the block
-  const int lane = tid & 31, warp = tid >> 5;
   int x = c;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -116,41 +119,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const float* __restr
   if (tid == kPlanThreads - 1) *count = warp_sums[31];
 }
 
-__global__ void __launch_bounds__(kPlanThreads) index_kernel(const uint8_t* __restrict__ flags, int n_mt, int n_vt,
-                                                             int kbt_dh, int kbt_dw, int* __restrict__ rowlist,
-                                                             int* __restrict__ rowcnt, int* __restrict__ collist,
-                                                             int* __restrict__ colcnt) {
-  for (int i = threadIdx.x; i < n_mt + n_vt; i += kPlanThreads) {
-    if (i < n_mt) {  // row tile mt: kept vocabulary tiles, 4 k-blocks each (the last tile may hold fewer)
-      const int mt = i;
-      int c = 0, last = -1;
-      for (int vt = 0; vt < n_vt; ++vt)
-        if (flags[mt * n_vt + vt]) rowlist[mt * n_vt + c++] = last = vt;
-      rowcnt[mt] = c * 4 - (last == n_vt - 1 ? n_vt * 4 - kbt_dh : 0);
-    } else {  // vocabulary tile vt: kept row tiles, 2 k-blocks each (the last may hold fewer)
-      const int vt = i - n_mt;
-      int c = 0, last = -1;
-      for (int mt = 0; mt < n_mt; ++mt)
-        if (flags[mt * n_vt + vt]) collist[vt * n_mt + c++] = last = mt;
-      colcnt[vt] = c * 2 - (last == n_mt - 1 ? n_mt * 2 - kbt_dw : 0);
-    }
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_skip_plan(const SkipPlan& P, cudaStream_t st) {
   prof_begin(K_SKIP, st);
-  plan_kernel<<<1, kPlanThreads, 0, st>>>(P.g, P.mask, P.targets, P.lse, P.bmax, P.bmax_ld, P.m0, P.mc, P.v0, P.vc,
-                                          P.n_mt, P.n_vt, P.M, P.V, P.thr2, P.list, P.count, P.flags, P.status);
-  prof_end(K_SKIP, st);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_skip_index(const SkipPlan& P, cudaStream_t st) {
-  prof_begin(K_SKIP, st);
-  index_kernel<<<1, kPlanThreads, 0, st>>>(P.flags, P.n_mt, P.n_vt, (P.vc + 63) / 64, (P.mc + 63) / 64, P.rowlist,
-                                           P.rowcnt, P.collist, P.colcnt);
+  plan_kernel<<<P.nblocks, kPlanThreads, 0, st>>>(P);
   prof_end(K_SKIP, st);
   return cudaGetLastError();
 }
