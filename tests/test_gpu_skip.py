@@ -162,3 +162,28 @@ def test_multiblock_skip_on_sampled_tiles():
             assert not dW[c0:c0 + 256].any()
         else:
             assert relfro(dW[c0:c0 + 256], rdW) < GRAD_RELFRO
+
+
+def test_plan_rounds_beyond_one_slot_area():
+    # 8 row blocks x 32 vocabulary blocks = 256 blocks; at 17.25 KiB a slot, the 4 MiB skip area holds
+    # 237, so the plan runs in two rounds and slots are reused
+    M, d, V = 131072, 64, 262144
+    w = workloads.make("e4b_sharp", M=M, d=d, V=V)
+    assert w.M == M
+    t = to_dev(w)
+    _, lse, bm, st = fwd_bmax(t, w.M, w.V, w.d, 30.0)
+    assert st == 0
+    g = (np.random.default_rng(8).standard_normal(w.M) * 1e-3 * (w.mask != 0)).astype(np.float32)
+    eps = 1e-5
+    dh, dW, st = bwd_skip(t, lse, g, bm, eps, w.M, w.V, w.d, 30.0)
+    dh1, dW1, st1 = bwd_skip(t, lse, g, None, eps, w.M, w.V, w.d, 30.0)
+    assert st == 0 and st1 == 0 and np.array_equal(dh, dh1) and np.array_equal(dW, dW1)
+    h, W = f64(w.h), f64(w.W)
+    for mt in (0, 900, w.M // 128 - 1):               # row tiles in the first and the second round
+        r = slice(128 * mt, 128 * mt + 128)
+        rdh, _ = oracle.head_backward(h[r], W, w.targets[r], w.mask[r], lse[r], g[r], 30.0, filter_eps=eps)
+        assert relfro(dh[r], rdh) < GRAD_RELFRO
+    for vt in (0, 1023):
+        c0 = 256 * vt
+        _, rdW = oracle.head_backward(h, W, w.targets, w.mask, lse, g, 30.0, filter_eps=eps, vocab=(c0, c0 + 256))
+        assert relfro(dW[c0:c0 + 256], rdW) < GRAD_RELFRO
