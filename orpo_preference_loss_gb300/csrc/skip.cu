@@ -31,7 +31,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMargin = 1.f / 64.f;  // base-2 slack for the fp32 rounding of both sides of the bound
 constexpr int kPlanThreads = 1024;
 constexpr int kGroupsMax = kMcMax / 32;
-static_assert(kMaxTiles == 4 * kPlanThreads, "the plan judges four tiles per thread");
+constexpr int kPerThread = kMaxTiles / kPlanThreads;  // tiles each thread judges
+static_assert(kMaxTiles == kPerThread * kPlanThreads, "tiles split evenly over the plan's threads");
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const SkipPlan P) {
   __shared__ uint8_t hot[kMaxTiles];        // [mt][vt]: a target of an active row lies in the tile
@@ -74,12 +75,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const SkipPlan P) {
     if (lane == 0) minlse2[r / 32] = l2;
   }
   __syncthreads();
-  // each thread judges 4 consecutive tiles in list order (u = vt * n_mt + mt), then a block scan
-  // gives their places in the list
-  int keep[4], c = 0;
+  // each thread judges kPerThread consecutive tiles in list order (u = vt * n_mt + mt), then a
+  // block scan gives their places in the list
+  int keep[kPerThread], c = 0;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int u = 4 * tid + k;
+  for (int k = 0; k < kPerThread; ++k) {
+    const int u = kPerThread * tid + k;
     keep[k] = 0;
     if (u >= ntiles) continue;
     const int vt = u / n_mt, mt = u - vt * n_mt;
@@ -114,8 +115,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const SkipPlan P) {
   __syncthreads();
   int pos = x - c + (warp > 0 ? warp_sums[warp - 1] : 0);
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    if (keep[k]) list[pos++] = 4 * tid + k;
+  for (int k = 0; k < kPerThread; ++k)
+    if (keep[k]) list[pos++] = kPerThread * tid + k;
   if (tid == kPlanThreads - 1) *count = warp_sums[31];
 }
 
