@@ -270,6 +270,7 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   void* Wb = q ? wblock_ptr(workspace, M, V) : nullptr;
   const FwdShape fs = forward_shape(n_mt, sms);
   L.pair = fs.pair;
+  L.chunk = l2_chunk((int)fs.units_m, (int64_t)(fs.pair ? 2 : 1) * kBM * d * 2);
   const uint32_t w_box = fs.pair ? kBN / 2 : kBN;
   int split0 = 0;
   for (int64_t v0 = 0; v0 < V; v0 += vb) {
@@ -331,6 +332,7 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
     P.shape = skip_shape(B);
     P.area = reinterpret_cast<uint8_t*>(counters + kCounters);
     P.thr2 = log2f(eps);
+    P.chunk_bytes = (int64_t)kBM * d * 2;
     if ((int64_t)P.shape.n_mt * P.shape.n_vt > kMaxTiles) return ORPO_ERR_SHAPE;  // cannot happen: Mc Vc bounded
     round_slots = (int)std::min<int64_t>(nblocks_all, (int64_t)(kSkipBytes / P.shape.slot_bytes));
   }
@@ -387,6 +389,7 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
       R.w_row0 = q ? 0 : (int)v0;
       R.n_mt = n_mt;
       R.n_vt = n_vt;
+      R.chunk = l2_chunk(n_mt, (int64_t)kBM * d * 2);
       R.grid = (int)std::min<int64_t>((int64_t)n_mt * n_vt, sms);
       uint32_t *rowbits = nullptr, *colbits = nullptr;
       if (skip) {

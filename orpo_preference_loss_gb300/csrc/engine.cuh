@@ -168,6 +168,24 @@ __device__ __forceinline__ uint8_t* smem_base_aligned() {
   return reinterpret_cast<uint8_t*>(p);
 }
 
+// L2-aware unit order over an (m, n) grid of units: m in chunks of `chunk`, and within a chunk
+// n-major (all m of the chunk for n = 0, then n = 1, ...).  Units that run at the same time then
+// share a few n (the same W tiles) and at most `chunk` m (the same rows of h), so both stay in L2.
+// chunk >= n_m gives the plain n-major order.
+__device__ __forceinline__ void chunk_decode(int u, int n_m, int n_n, int chunk, int& m, int& n) {
+  if (chunk >= n_m) {  // one chunk: plain n-major order
+    n = u / n_m;
+    m = u - n * n_m;
+    return;
+  }
+  const int per = chunk * n_n;
+  const int c = u / per;
+  const int local = u - c * per;
+  const int rc = min(chunk, n_m - c * chunk);
+  n = local / rc;
+  m = c * chunk + (local - n * rc);
+}
+
 // Bounded wait on an mbarrier phase.  Returns false on abort / timeout.
 __device__ __forceinline__ bool wait_phase(SmemCtl* ctl, uint64_t* bar, uint32_t parity, int32_t* status,
                                            uint64_t limit_ns) {

@@ -26,10 +26,16 @@ struct RecSched {
   const CUtensorMap* mw;
   int m0, v0, n_mt, n_vt, kblocks;
   int w_row0;        // row of the W map that holds vocabulary column v0
-  const int* list;   // backward skips: the tiles to compute (vt * n_mt + mt, ascending), or nullptr for all
+  const int* list;   // backward skips: the tiles to compute (vt * n_mt + mt, in unit order), or nullptr
   const int* count;  // number of entries of list
+  int chunk;         // row tiles per L2 chunk (chunk_decode)
   __device__ int num_units() const { return list ? __ldg(count) : n_mt * n_vt; }
-  __device__ int tile_index(int u) const { return list ? __ldg(list + u) : u; }
+  __device__ int tile_index(int u) const {
+    if (list) return __ldg(list + u);
+    int mt, vt;
+    chunk_decode(u, n_mt, n_vt, chunk, mt, vt);
+    return vt * n_mt + mt;
+  }
   __device__ int unit_len(int) const { return 1; }
   __device__ TileOps tile(int u, int) const {
     const int x = tile_index(u);
@@ -402,7 +408,8 @@ template <int cap, bool kFilter>
 cudaError_t launch_rec_kernel(const RecLaunch& L, cudaStream_t st) {
   static int smem_set[64] = {0};
   if (cudaError_t e = opt_in_smem(rec_kernel<cap, kFilter>, SMEM_TOTAL, smem_set)) return e;
-  RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks, L.w_row0, L.list, L.count};
+  const int chunk = L.chunk > 0 && L.chunk < L.n_mt ? L.chunk : L.n_mt;
+  RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks, L.w_row0, L.list, L.count, chunk};
   RecArgs a{L.targets, L.mask, L.lse, L.g, L.M, L.V, L.softcap, L.status, L.eps, L.rowbits, L.colbits, L.ld_row,
             L.ld_col};
   prof_begin(K_REC, st);

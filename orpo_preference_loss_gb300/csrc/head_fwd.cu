@@ -28,12 +28,18 @@ struct FwdSched {
   const CUtensorMap* mh;
   const CUtensorMap* mw;
   int n_mt, nsplit, n_vt, kblocks;  // pair mode: n_mt is even
+  int chunk;                        // units along M per L2 chunk (chunk_decode)
   int pair, rank;                   // pair mode flag; this CTA's rank in its cluster (0 otherwise)
   __device__ int n_mu() const { return pair ? n_mt >> 1 : n_mt; }
   __device__ int num_units() const { return n_mu() * nsplit; }
-  __device__ int split_of(int u) const { return u / n_mu(); }
+  __device__ int split_of(int u) const {
+    int m, s;
+    chunk_decode(u, n_mu(), nsplit, chunk, m, s);
+    return s;
+  }
   __device__ int mt_of(int u) const {
-    const int m = u - split_of(u) * n_mu();
+    int m, s;
+    chunk_decode(u, n_mu(), nsplit, chunk, m, s);
     return pair ? 2 * m + rank : m;
   }
   __device__ int vt_begin(int s) const { return (int)(((long long)s * n_vt) / nsplit); }
@@ -248,7 +254,9 @@ cudaError_t launch_fwd_kernel(const FwdLaunch& L, cudaStream_t st) {
   static int smem_set[64] = {0};
   if (cudaError_t e = opt_in_smem(fwd_kernel<cap, kPair>, SMEM_TOTAL, smem_set)) return e;
   const int n_mt = kPair ? (L.n_mt + 1) & ~1 : L.n_mt;
-  FwdSched sched{nullptr, nullptr, n_mt, L.nsplit, L.n_vt, L.kblocks, 0, 0};
+  const int n_mu = kPair ? n_mt / 2 : n_mt;
+  const int chunk = L.chunk > 0 && L.chunk < n_mu ? L.chunk : n_mu;
+  FwdSched sched{nullptr, nullptr, n_mt, L.nsplit, L.n_vt, L.kblocks, chunk, 0, 0};
   FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M,      L.Mpad,
             L.V,       L.softcap, L.status, L.col0, L.split0, L.bmax, (L.V + BN - 1) / BN};
   cudaError_t e = cudaSuccess;

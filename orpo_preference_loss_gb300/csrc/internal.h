@@ -32,6 +32,17 @@ constexpr int64_t kMcMax = 16384; // rows per backward block
 constexpr int64_t kScratchBudget = 256ll << 20;  // bytes of the bf16 dZ block
 constexpr int kMaxTiles = (int)(kScratchBudget / 2 / (kBM * kBN));  // 128 x 256 tiles in one dZ block
 
+// ---- L2-aware unit order (chunk_decode in engine.cuh): units along M per chunk.  The rows of h
+// that concurrently running units re-read (one 128-row tile, or a pair, per M unit) are kept within
+// kL2ChunkBytes; the chunks are then made about equal.
+constexpr int64_t kL2ChunkBytes = 48ll << 20;
+__host__ __device__ inline int l2_chunk(int n_m, int64_t bytes_per_m) {
+  const int64_t rmax = bytes_per_m > 0 ? (kL2ChunkBytes / bytes_per_m > 1 ? kL2ChunkBytes / bytes_per_m : 1) : n_m;
+  if (rmax >= n_m) return n_m > 0 ? n_m : 1;
+  const int64_t nc = (n_m + rmax - 1) / rmax;
+  return (int)((n_m + nc - 1) / nc);
+}
+
 // ---- forward
 struct FwdLaunch {
   CUtensorMap mh, mw;  // h K-major box {64,128}; W K-major box {64,256}
@@ -50,6 +61,7 @@ struct FwdLaunch {
   int split0 = 0;  // first split index this launch writes
   int pair = 0;    // 1: 2-CTA clusters share W tiles (mw box {64,128}; grid = 2 x clusters; n_mt padded to even)
   float* bmax = nullptr;  // optional block maxima [ceil(M/32), ceil(V/256)] (base-2 softcapped logits)
+  int chunk = 0;          // M units per L2 chunk (l2_chunk); 0: all of them
 };
 int forward_pair_clusters();  // co-resident 2-CTA clusters of the forward kernel (0: pair mode unavailable)
 cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st);  // logits kernel + merge of L.nsplit splits
@@ -76,6 +88,7 @@ struct RecLaunch {
   uint32_t* colbits = nullptr;  // or nullptr for no filter
   int ld_row = 0, ld_col = 0;
   float eps = 0.f;
+  int chunk = 0;                // row tiles per L2 chunk (l2_chunk); 0: all of them
 };
 cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st);
 
@@ -108,6 +121,7 @@ struct SkipPlan {
   uint8_t* area;      // slot s at area + s * shape.slot_bytes
   float thr2;         // log2(eps)
   int32_t* status;
+  int64_t chunk_bytes;  // h bytes per row tile: the list follows the recompute's l2_chunk order
 };
 cudaError_t launch_skip_plan(const SkipPlan& P, cudaStream_t st);  // lists and zeroed bitmaps for a round
 

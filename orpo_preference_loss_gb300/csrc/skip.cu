@@ -15,8 +15,9 @@
 // tile) - (smallest lse of the group's rows with g != 0) lies below
 // log2(eps) - kMargin in base-2 units, which bounds every p sech^2 of the tile
 // below eps.  The filter would drop every cold tile anyway, so the block skip
-// leaves the result unchanged.  The list is vocabulary-tile-major and
-// ascending, the order of the full recompute.
+// leaves the result unchanged.  The list follows the full recompute's unit
+// order (row-tile chunks, vocabulary-tile-major within a chunk).
+#include "engine.cuh"
 #include "internal.h"
 
 #include <cuda_runtime.h>
@@ -75,15 +76,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const SkipPlan P) {
     if (lane == 0) minlse2[r / 32] = l2;
   }
   __syncthreads();
-  // each thread judges kPerThread consecutive tiles in list order (u = vt * n_mt + mt), then a
-  // block scan gives their places in the list
+  // each thread judges kPerThread consecutive tiles in the recompute's unit order (chunk_decode),
+  // then a block scan gives their places in the list, which holds tile ids vt * n_mt + mt
+  const int chunk = l2_chunk(n_mt, P.chunk_bytes);
   int keep[kPerThread], c = 0;
 #pragma unroll
   for (int k = 0; k < kPerThread; ++k) {
     const int u = kPerThread * tid + k;
     keep[k] = 0;
     if (u >= ntiles) continue;
-    const int vt = u / n_mt, mt = u - vt * n_mt;
+    int mt, vt;
+    chunk_decode(u, n_mt, n_vt, chunk, mt, vt);
     int hit = hot[mt * n_vt + vt];
     for (int gq = mt * 4; !hit && gq < min(ngroups, mt * 4 + 4); ++gq) {
       const float ml = minlse2[gq];
@@ -115,8 +118,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const SkipPlan P) {
   __syncthreads();
   int pos = x - c + (warp > 0 ? warp_sums[warp - 1] : 0);
 #pragma unroll
-  for (int k = 0; k < kPerThread; ++k)
-    if (keep[k]) list[pos++] = kPerThread * tid + k;
+  for (int k = 0; k < kPerThread; ++k) {
+    if (!keep[k]) continue;
+    int mt, vt;
+    chunk_decode(kPerThread * tid + k, n_mt, n_vt, chunk, mt, vt);
+    list[pos++] = vt * n_mt + mt;
+  }
   if (tid == kPlanThreads - 1) *count = warp_sums[31];
 }
 
