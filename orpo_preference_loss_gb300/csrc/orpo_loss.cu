@@ -31,6 +31,9 @@ namespace {
 
 constexpr int T = 1024;
 constexpr int kKindOrpo = 0, kKindSimpo = 1, kKindDpo = 2, kKindIpo = 3, kKindHinge = 4, kKindOrpoFull = 5;
+static_assert(kKindOrpo == ORPO_PREF_ORPO && kKindSimpo == ORPO_PREF_SIMPO && kKindDpo == ORPO_PREF_DPO &&
+                  kKindIpo == ORPO_PREF_IPO && kKindHinge == ORPO_PREF_HINGE && kKindOrpoFull == ORPO_PREF_ORPO_FULL,
+              "kernel kinds are the ABI's ORPO_PREF_* values");
 constexpr uint8_t kPromptRow = 2;  // mask value: prompt row, supervised only by the full-scope NLL
 constexpr int32_t kSeqErr = ORPO_STATUS_SEQID, kEmptyErr = ORPO_STATUS_EMPTY_SEQ,
                   kNonfiniteErr = ORPO_STATUS_NONFINITE;
