@@ -8,7 +8,9 @@
 // bounded bf16 buffer that the bf16 tensor-core kernels then read.  The weight is
 // W[v, j] = bf16(scale[v, j/group] * q[v, j] + bias[v, j/group]) (fp32 arithmetic,
 // one nearest-even rounding); 4-bit q are packed two per byte, even column low.
-// Memory-bound: reads bits/8 + 4/group bytes and writes 2 bytes per weight.
+// Memory-bound: reads bits/8 + 4/group bytes and writes 2 bytes per weight.  4-bit rows are read as
+// 32-bit words and 8-bit rows as 64-bit words: wq is 4- (4-bit) or 8-byte (8-bit) aligned and d is a
+// multiple of 8 (checked by the host).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -36,41 +38,51 @@ __device__ __forceinline__ uint4 dequant8(const uint32_t (&q)[8], float s, float
   return o;
 }
 
-// one thread: kSpan consecutive weights of one row (kSpan / 8 sixteen-byte stores); kSpan is 32
-// when d % 32 == 0 (wider loads, more bytes in flight per thread), else 8
-template <int kBits, int kSpan>
-__global__ void dequant_kernel(const uint8_t* __restrict__ wq, const uint16_t* __restrict__ scales,
-                               const uint16_t* __restrict__ biases, int group, int64_t v0, int64_t rows, int64_t d,
-                               uint4* __restrict__ out) {
-  const int64_t per_row = d / kSpan;
-  const int64_t n = rows * per_row;
-  const int64_t ngroups = d / group;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / per_row, c = i - r * per_row;
-    const int64_t v = v0 + r, j0 = c * kSpan;
-    uint32_t words[kSpan * kBits / 32];
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(wq + v * (d * kBits / 8) + j0 * kBits / 8);
-    if constexpr (kSpan * kBits / 32 % 4 == 0) {
+// Slice = 8 consecutive weights of a row (one 16-byte bf16 store).  Thread t of T handles slices
+// t, t + T, t + 2T, t + 3T per trip, so a warp's 32 stores of one round cover 512 contiguous bytes
+// and four independent loads are in flight per thread.  A block holds at most kWBlockBudget bytes
+// of bf16 (rows * d / 8 < 2^31 slices), so slice indices fit 32 bits.
+constexpr int kUnroll = 4;
+
+template <int kBits>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ wq,
+                                                      const uint16_t* __restrict__ scales,
+                                                      const uint16_t* __restrict__ biases, int group, int64_t v0,
+                                                      int rows, int d, uint4* __restrict__ out) {
+  const uint32_t per_row = (uint32_t)d / 8u;
+  const uint32_t nslices = (uint32_t)rows * per_row;
+  const uint32_t ngroups = (uint32_t)(d / group);
+  const uint32_t T = gridDim.x * blockDim.x;
+  for (uint32_t base = blockIdx.x * blockDim.x + threadIdx.x; base < nslices; base += kUnroll * T) {
+    uint2 raw[kUnroll];
+    float sc[kUnroll], bi[kUnroll];
 #pragma unroll
-      for (int k = 0; k < kSpan * kBits / 128; ++k) {
-        const uint4 x = reinterpret_cast<const uint4*>(src)[k];
-        words[4 * k] = x.x, words[4 * k + 1] = x.y, words[4 * k + 2] = x.z, words[4 * k + 3] = x.w;
+    for (int k = 0; k < kUnroll; ++k) {
+      const uint32_t idx = base + k * T;
+      raw[k] = make_uint2(0u, 0u);
+      sc[k] = bi[k] = 0.f;
+      if (idx < nslices) {
+        const uint32_t r = idx / per_row, c = idx - r * per_row;
+        const int64_t v = v0 + r;
+        const uint8_t* row = wq + v * (int64_t)(d * kBits / 8);
+        if constexpr (kBits == 4)
+          raw[k].x = __ldg(reinterpret_cast<const uint32_t*>(row) + c);
+        else
+          raw[k] = __ldg(reinterpret_cast<const uint2*>(row) + c);
+        const int64_t gi = v * ngroups + (8u * c) / (uint32_t)group;
+        sc[k] = bf16_bits_to_float(__ldg(scales + gi));
+        bi[k] = bf16_bits_to_float(__ldg(biases + gi));
       }
-    } else {
-#pragma unroll
-      for (int k = 0; k < kSpan * kBits / 32; ++k) words[k] = src[k];
     }
 #pragma unroll
-    for (int sub = 0; sub < kSpan / 8; ++sub) {
-      const int64_t gi = v * ngroups + (j0 + 8 * sub) / group;
-      const float s = bf16_bits_to_float(scales[gi]), b = bf16_bits_to_float(biases[gi]);
+    for (int k = 0; k < kUnroll; ++k) {
+      const uint32_t idx = base + k * T;
+      if (idx >= nslices) break;
       uint32_t q[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int e = 8 * sub + k;  // element within the span
-        q[k] = kBits == 4 ? (words[e / 8] >> (4 * (e % 8))) & 15u : (words[e / 4] >> (8 * (e % 4))) & 255u;
-      }
-      out[(r * d + j0) / 8 + sub] = dequant8(q, s, b);
+      for (int e = 0; e < 8; ++e)
+        q[e] = kBits == 4 ? (raw[k].x >> (4 * e)) & 15u : ((e < 4 ? raw[k].x : raw[k].y) >> (8 * (e & 3))) & 255u;
+      out[idx] = dequant8(q, sc[k], bi[k]);  // slices are row-major over [rows, d]
     }
   }
 }
@@ -79,23 +91,18 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ wq, const uint16_t* _
 
 cudaError_t launch_dequant(const uint8_t* wq, const void* scales, const void* biases, int bits, int group,
                            int64_t v0, int64_t rows, int64_t d, void* out_bf16, cudaStream_t st) {
-  // 32 weights per thread needs 16-byte loads: d % 32 == 0 keeps every row 16-byte aligned
-  const bool wide = d % 32 == 0 && (reinterpret_cast<uintptr_t>(wq) & 15u) == 0;
-  const int64_t n = rows * (d / (wide ? 32 : 8));
+  const int64_t n = rows * (d / 8);
+  if (n >= (1ll << 31)) return cudaErrorInvalidValue;  // cannot happen: a block is bounded by kWBlockBudget
   const int threads = 256;
-  const int64_t blocks = std::min<int64_t>((n + threads - 1) / threads, 152 * 16);
+  const int64_t blocks = std::min<int64_t>((n + threads * kUnroll - 1) / (threads * kUnroll), 152 * 16);
   const uint16_t* sc = static_cast<const uint16_t*>(scales);
   const uint16_t* bi = static_cast<const uint16_t*>(biases);
   uint4* o = static_cast<uint4*>(out_bf16);
   prof_begin(K_DEQUANT, st);
-  if (bits == 4 && wide)
-    dequant_kernel<4, 32><<<(int)blocks, threads, 0, st>>>(wq, sc, bi, group, v0, rows, d, o);
-  else if (bits == 4)
-    dequant_kernel<4, 8><<<(int)blocks, threads, 0, st>>>(wq, sc, bi, group, v0, rows, d, o);
-  else if (wide)
-    dequant_kernel<8, 32><<<(int)blocks, threads, 0, st>>>(wq, sc, bi, group, v0, rows, d, o);
+  if (bits == 4)
+    dequant_kernel<4><<<(int)blocks, threads, 0, st>>>(wq, sc, bi, group, v0, (int)rows, (int)d, o);
   else
-    dequant_kernel<8, 8><<<(int)blocks, threads, 0, st>>>(wq, sc, bi, group, v0, rows, d, o);
+    dequant_kernel<8><<<(int)blocks, threads, 0, st>>>(wq, sc, bi, group, v0, (int)rows, (int)d, o);
   prof_end(K_DEQUANT, st);
   return cudaGetLastError();
 }
