@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -45,6 +46,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the raw nvidia-smi clock samples of the timed region in this file")
     ap.add_argument("--loss", default="orpo", choices=["orpo", "simpo", "dpo", "ipo", "hinge", "orpo_full"],
                     help="preference objective between forward and backward (orpo_loss for orpo)")
     ap.add_argument("--quant", type=int, default=0, choices=[0, 4, 8],
@@ -125,10 +128,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, path=None):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = path or os.path.join(tempfile.gettempdir(), f"orpo_clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
@@ -320,7 +323,7 @@ def ours(args, w, rank, world, local):
             dist.barrier()
 
     # ---- device-timed region: inputs resident in HBM
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clocks_csv)
     clocks.start()
     barrier()
     torch.cuda.synchronize()

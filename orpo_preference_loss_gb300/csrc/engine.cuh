@@ -11,8 +11,12 @@
 //   K-major operand  [rows, K] with K contiguous: one TMA box {64 (K), rows};
 //                    rows at 128 B pitch, 8-row swizzle atoms 1024 B apart (SBO).
 //   MN-major operand [K, rows] with rows contiguous: rows/64 TMA boxes {64, 64},
-//                    each 64 k-rows x 128 B = 8 KiB; LBO = 8 KiB between 64-wide
-//                    column blocks, SBO = 1 KiB between 8-k-row groups.
+//                    each 64 k-rows x 128 B = 8 KiB (or one 3-D box over all of them);
+//                    LBO = 8 KiB between 64-wide column blocks, SBO = 1 KiB between
+//                    8-k-row groups.
+// Options a kernel picks: a paired mode (2-CTA clusters that multicast halves of the
+// B tile to each other, run_cta<true>), sparse K (a bitmap of k-block groups per tile,
+// KWalk), a static or a dynamic unit feed, and an L2-aware unit order (chunk_decode).
 // Every wait is bounded: a wait that exceeds kWaitLimitNs sets ORPO_STATUS_TIMEOUT,
 // flags the CTA as aborted and every role drains its own in-flight work and returns.
 #pragma once

@@ -3,9 +3,9 @@
 // Fused-head spec, backward bullet: recompute the vocabulary tiles, rebuild the
 // softmax from the saved lse, form g * (onehot - softmax) * sech^2 and contract
 // it into dh (and, here, dW).  The "Steel flash-CCE — handoff" page accumulated
-// dh with float atomics across vocabulary blocks; this build instead streams the
-// bf16 logit gradient of one (row block, vocabulary block) through a bounded
-// workspace block S and contracts it with two large-K GEMMs per block:
+// dh with float atomics across vocabulary blocks; here the bf16 logit gradient
+// of one (row block, vocabulary block) is streamed through a bounded workspace
+// block S and contracted with two large-K GEMMs per block:
 //   recompute kernel : S = bf16(dZ[m0:m0+Mc, v0:v0+Vc])             (K = d)
 //   gemm kernel      : dh[m0 rows]  (+)= S   W[v0 rows]             (K = Vc)
 //                      dW[v0 rows]  (+)= S^T h[m0 rows]             (K = Mc)
