@@ -8,6 +8,7 @@ is skipped when the library is newer than every source and header.
 
 from __future__ import annotations
 
+import fcntl
 import glob
 import os
 import shutil
@@ -51,10 +52,24 @@ def up_to_date() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library if needed; returns the path of the shared object."""
+    """Compile the library if needed; returns the path of the shared object.
+
+    Safe to call from several processes at once (ranks of one job): a file lock lets one of them
+    build while the others wait and then find the library up to date."""
     if not force and up_to_date():
         return LIB_PATH
     os.makedirs(OUT_DIR, exist_ok=True)
+    with open(os.path.join(OUT_DIR, ".build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and up_to_date():
+                return LIB_PATH
+            return _build_locked(verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose: bool) -> str:
     nvcc = nvcc_path()
     srcs = _sources()
     objs = [os.path.join(OUT_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
