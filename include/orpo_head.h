@@ -246,8 +246,13 @@ int orpo_head_bwd_q(const void* h_bf16, const uint8_t* wq, const void* scales_bf
  *   eps (0 <= eps, finite; eps = 0 is exactly orpo_head_bwd).  block_max, when
  *   not NULL, must be what orpo_head_fwd_bmax wrote for the same h, W, mask and
  *   softcap; it enables the block skip.  NULL runs the filter alone.
+ * orpo_head_fwd_q_bmax / orpo_head_bwd_q_skip: the same two calls for the
+ *   quantised head (arguments as orpo_head_fwd_q / orpo_head_bwd_q, workspace
+ *   orpo_head_q_workspace_bytes); the skips then act on the dequantised weight.
+ *   The pages run their head this way: quantised, with the skips on.
  * Host errors: ORPO_ERR_ARG for a negative or non-finite eps; otherwise those
- * of orpo_head_fwd / orpo_head_bwd.  The workspace is orpo_head_workspace_bytes.
+ * of orpo_head_fwd / orpo_head_bwd (or their quantised forms).  The workspace
+ * is orpo_head_workspace_bytes (orpo_head_q_workspace_bytes when quantised).
  */
 size_t orpo_head_block_max_elems(int64_t M, int64_t V);
 int orpo_head_fwd_bmax(const void* h_bf16, const void* W_bf16, const int32_t* targets,
@@ -259,6 +264,17 @@ int orpo_head_bwd_skip(const void* h_bf16, const void* W_bf16, const int32_t* ta
                        float eps, int64_t M, int64_t V, int64_t d, float softcap, float* dh,
                        float* dW, int accumulate_dW, void* workspace, size_t ws_bytes,
                        int32_t* status, void* stream);
+int orpo_head_fwd_q_bmax(const void* h_bf16, const uint8_t* wq, const void* scales_bf16,
+                         const void* biases_bf16, int bits, int group, const int32_t* targets,
+                         const uint8_t* mask, int64_t M, int64_t V, int64_t d, float softcap,
+                         float* logp, float* lse, float* block_max, void* workspace,
+                         size_t ws_bytes, int32_t* status, void* stream);
+int orpo_head_bwd_q_skip(const void* h_bf16, const uint8_t* wq, const void* scales_bf16,
+                         const void* biases_bf16, int bits, int group, const int32_t* targets,
+                         const uint8_t* mask, const float* lse, const float* g,
+                         const float* block_max, float eps, int64_t M, int64_t V, int64_t d,
+                         float softcap, float* dh, float* dW, int accumulate_dW, void* workspace,
+                         size_t ws_bytes, int32_t* status, void* stream);
 
 /* Text of a return code or of a set of ORPO_STATUS_* bits (static storage). */
 const char* orpo_status_string(int code);

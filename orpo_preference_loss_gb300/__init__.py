@@ -82,6 +82,12 @@ def load():
     L.orpo_head_bwd_skip.argtypes = [vp, vp, vp, vp, vp, vp, vp, f32, i64, i64, i64, f32, vp, vp, ctypes.c_int, vp,
                                      sz, vp, vp]
     L.orpo_head_bwd_skip.restype = ctypes.c_int
+    L.orpo_head_fwd_q_bmax.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, vp, vp, i64, i64, i64, f32, vp,
+                                       vp, vp, vp, sz, vp, vp]
+    L.orpo_head_fwd_q_bmax.restype = ctypes.c_int
+    L.orpo_head_bwd_q_skip.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, f32, i64, i64,
+                                       i64, f32, vp, vp, ctypes.c_int, vp, sz, vp, vp]
+    L.orpo_head_bwd_q_skip.restype = ctypes.c_int
     L.orpo_profile_start.argtypes = []
     L.orpo_profile_start.restype = ctypes.c_int
     L.orpo_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), ctypes.c_int]
@@ -317,6 +323,46 @@ def orpo_head_bwd_q(h, wq, scales, biases, bits, group, targets, mask, lse, g, s
                                   _ptr(mask), _ptr(lse), _ptr(g), M, V, d, float(softcap), _ptr(dh), _ptr(dW),
                                   1 if accumulate_dW else 0, _ptr(workspace), workspace.numel(), _ptr(status),
                                   _stream(stream)), "orpo_head_bwd_q")
+
+
+def orpo_head_fwd_q_bmax(h, wq, scales, biases, bits, group, targets, mask, softcap, logp, lse, block_max,
+                         workspace, status, stream=None):
+    """orpo_head_fwd_q that also writes the block maxima of the backward skips."""
+    M, d = h.shape
+    V = wq.shape[0]
+    _dev(h, "h", BF16)
+    _quant_args(wq, scales, biases, V, d, bits, group)
+    _dev(targets, "targets", (torch.int32,), (M,))
+    _dev(mask, "mask", (torch.uint8, torch.bool), (M,))
+    _dev(logp, "logp", (torch.float32,), (M,))
+    _dev(lse, "lse", (torch.float32,), (M,))
+    _dev(block_max, "block_max", (torch.float32,), block_max_shape(M, V))
+    _dev(workspace, "workspace", (torch.uint8,))
+    _check(load().orpo_head_fwd_q_bmax(_ptr(h), _ptr(wq), _ptr(scales), _ptr(biases), int(bits), int(group),
+                                       _ptr(targets), _ptr(mask), M, V, d, float(softcap), _ptr(logp), _ptr(lse),
+                                       _ptr(block_max), _ptr(workspace), workspace.numel(), _ptr(status),
+                                       _stream(stream)), "orpo_head_fwd_q_bmax")
+
+
+def orpo_head_bwd_q_skip(h, wq, scales, biases, bits, group, targets, mask, lse, g, block_max, eps, softcap, dh, dW,
+                         accumulate_dW, workspace, status, stream=None):
+    """orpo_head_bwd_q with the backward skips (block_max may be None: filter alone)."""
+    M, d = h.shape
+    V = wq.shape[0]
+    _dev(h, "h", BF16)
+    _quant_args(wq, scales, biases, V, d, bits, group)
+    _dev(lse, "lse", (torch.float32,), (M,))
+    _dev(g, "g", (torch.float32,), (M,))
+    if block_max is not None:
+        _dev(block_max, "block_max", (torch.float32,), block_max_shape(M, V))
+    _dev(dh, "dh", (torch.float32,), (M, d))
+    if dW is not None:
+        _dev(dW, "dW", (torch.float32,), (V, d))
+    _check(load().orpo_head_bwd_q_skip(_ptr(h), _ptr(wq), _ptr(scales), _ptr(biases), int(bits), int(group),
+                                       _ptr(targets), _ptr(mask), _ptr(lse), _ptr(g), _ptr(block_max), float(eps), M, V,
+                                       d, float(softcap), _ptr(dh), _ptr(dW), 1 if accumulate_dW else 0,
+                                       _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)),
+           "orpo_head_bwd_q_skip")
 
 
 def orpo_debug_gemm(A, B, C, M, N, K, a_mn_major, b_mn_major, status, stream=None):

@@ -557,6 +557,28 @@ int orpo_head_bwd_skip(const void* h, const void* W, const int32_t* targets, con
                        accumulate_dW, workspace, ws_bytes, status, stream);
 }
 
+int orpo_head_fwd_q_bmax(const void* h, const uint8_t* wq, const void* scales, const void* biases, int bits,
+                         int group, const int32_t* targets, const uint8_t* mask, int64_t M, int64_t V, int64_t d,
+                         float softcap, float* logp, float* lse, float* block_max, void* workspace, size_t ws_bytes,
+                         int32_t* status, void* stream) {
+  if (M > 0 && !block_max) return ORPO_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(block_max) & 3u) return ORPO_ERR_ALIGN;
+  const QuantW q{wq, scales, biases, bits, group};
+  return head_fwd_impl(h, nullptr, &q, targets, mask, M, V, d, softcap, logp, lse, block_max, workspace, ws_bytes,
+                       status, stream);
+}
+
+int orpo_head_bwd_q_skip(const void* h, const uint8_t* wq, const void* scales, const void* biases, int bits,
+                         int group, const int32_t* targets, const uint8_t* mask, const float* lse, const float* g,
+                         const float* block_max, float eps, int64_t M, int64_t V, int64_t d, float softcap, float* dh,
+                         float* dW, int accumulate_dW, void* workspace, size_t ws_bytes, int32_t* status,
+                         void* stream) {
+  if (reinterpret_cast<uintptr_t>(block_max) & 3u) return ORPO_ERR_ALIGN;
+  const QuantW q{wq, scales, biases, bits, group};
+  return head_bwd_impl(h, nullptr, &q, targets, mask, lse, g, block_max, eps, M, V, d, softcap, dh, dW,
+                       accumulate_dW, workspace, ws_bytes, status, stream);
+}
+
 int orpo_debug_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int a_mn_major,
                     int b_mn_major, int32_t* status, void* stream) {
   if (M < 1 || N < 1 || K < 1 || M > kMaxRows || N > kMaxRows || K > kMaxRows) return ORPO_ERR_SHAPE;

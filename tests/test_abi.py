@@ -132,3 +132,18 @@ def test_skip_host_checks(lib):
     assert bwd_skip(eps=float("inf")) == ERR_ARG
     assert bwd_skip(bm=ctypes.c_void_p(0x10002)) == ERR_ALIGN
     assert bwd_skip(ws=8) == ERR_WS
+
+
+def test_quantised_skip_host_checks(lib):
+    def fwd(bm=FAKE, M=64):
+        return lib.orpo_head_fwd_q_bmax(FAKE, FAKE, FAKE, FAKE, 4, 64, FAKE, FAKE, M, 128, 64, 0.0, FAKE, FAKE, bm,
+                                        FAKE, 1 << 30, FAKE, None)
+
+    def bwd(eps=1e-5, bits=4):
+        return lib.orpo_head_bwd_q_skip(FAKE, FAKE, FAKE, FAKE, bits, 64, FAKE, FAKE, FAKE, FAKE, FAKE, eps, 64, 128,
+                                        64, 0.0, FAKE, FAKE, 0, FAKE, 1 << 30, FAKE, None)
+
+    assert fwd(bm=None) == ERR_NULL
+    assert fwd(bm=ctypes.c_void_p(0x10002)) == ERR_ALIGN
+    assert bwd(eps=-1.0) == ERR_ARG
+    assert bwd(bits=5) == ERR_ARG

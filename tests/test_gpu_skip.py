@@ -187,3 +187,47 @@ def test_plan_rounds_beyond_one_slot_area():
         c0 = 256 * vt
         _, rdW = oracle.head_backward(h, W, w.targets, w.mask, lse, g, 30.0, filter_eps=eps, vocab=(c0, c0 + 256))
         assert relfro(dW[c0:c0 + 256], rdW) < GRAD_RELFRO
+
+
+def test_quantised_head_with_skips():
+    # the pages' own configuration: a 4-bit head with the skips on; checked against the oracle on the
+    # dequantised weights
+    w = workloads.make("e4b_sharp", M=512, d=256, V=65536)
+    bits, group, softcap, eps = 4, 64, 30.0, 1e-5
+    wq, s, b = workloads.quantize_affine(w.W, bits, group)
+    Wd = oracle.dequant_affine(wq, s, b, bits, group, w.d)
+    t = to_dev(w)
+    q = (torch.from_numpy(wq).to(dev()), torch.from_numpy(s.view(np.int16)).to(dev()).view(torch.bfloat16),
+         torch.from_numpy(b.view(np.int16)).to(dev()).view(torch.bfloat16))
+    M, V, d = w.M, w.V, w.d
+    ws = torch.empty(orpo.orpo_head_q_workspace_bytes(M, V, d), dtype=torch.uint8, device=dev())
+    st = status_tensor()
+    logp = torch.empty(M, device=dev())
+    lse = torch.empty(M, device=dev())
+    bm = torch.full(orpo.block_max_shape(M, V), float("nan"), device=dev())
+    orpo.orpo_head_fwd_q_bmax(t["h"], *q, bits, group, t["targets"], t["mask"], softcap, logp, lse, bm, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    h = f64(w.h)
+    logp_r, lse_r = oracle.head_forward(h, Wd, w.targets, w.mask, softcap)
+    assert np.max(np.abs(lse.cpu().numpy() - lse_r)) < LOGP_ATOL
+    ref_bm = oracle.head_block_max(h, Wd, w.mask, softcap)
+    got_bm = bm.cpu().numpy()
+    fin = np.isfinite(ref_bm)
+    assert np.array_equal(np.isneginf(got_bm), np.isneginf(ref_bm))
+    assert np.max(np.abs(got_bm[fin] - ref_bm[fin])) < LOGP_ATOL * LOG2E
+    g = orpo_g(w, logp_r).astype(np.float32)
+    lse32 = lse_r.astype(np.float32)
+    grads = []
+    for use_bm in (True, False):
+        dh = torch.empty((M, d), device=dev())
+        dW = torch.empty((V, d), device=dev())
+        orpo.orpo_head_bwd_q_skip(t["h"], *q, bits, group, t["targets"], t["mask"], torch.from_numpy(lse32).to(dev()),
+                                  torch.from_numpy(g).to(dev()), bm if use_bm else None, eps, softcap, dh, dW, False,
+                                  ws, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        grads.append((dh.cpu().numpy(), dW.cpu().numpy()))
+    rdh, rdW = oracle.head_backward(h, Wd, w.targets, w.mask, lse32, g, softcap, filter_eps=eps)
+    assert relfro(grads[0][0], rdh) < GRAD_RELFRO and relfro(grads[0][1], rdW) < GRAD_RELFRO
+    assert np.array_equal(grads[0][0], grads[1][0]) and np.array_equal(grads[0][1], grads[1][1])
