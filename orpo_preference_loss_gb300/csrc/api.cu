@@ -294,6 +294,47 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   return launch_forward_merge(L, split0, st) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
 }
 
+// The two GEMM classes of one backward block (gemm maps: 0 S K-major rows, 1 W MN-major, 2 S MN-major,
+// 3 h MN-major, 4 dh, 5 dW).  With keep bitmaps (backward skips) K runs over the kept tiles only.
+
+// dW[v0 + ..] (+)= S^T h[m0 + ..]: 128-column tiles of S against h, K = the block's rows
+GemmClassH dw_class(int64_t v0, int64_t vc, int64_t m0, int64_t mc, int64_t V, int64_t d, int accumulate,
+                    const uint32_t* colbits, int ld_col) {
+  GemmClassH c{};
+  c.a_map = 2, c.a_mn = 2, c.a_mn_base = 0, c.a_k_base = 0;
+  c.b_map = 3, c.b_mn = d % 64 == 0 ? 2 : 1, c.b_mn_base = 0, c.b_k_base = (int)m0;
+  c.out_map = 5, c.out_row_base = (int)v0, c.out_col_base = 0;
+  c.reduce = (m0 > 0 || accumulate) ? 1 : 0;  // the first row block stores, later ones add
+  c.out_rows = (int)V, c.out_cols = (int)d;
+  c.n_mt = (int)cdiv(vc, kBM), c.n_nt = (int)cdiv(d, kBN), c.kblocks = (int)cdiv(mc, 64);
+  c.mt_major = 1;  // CTAs running together share one column slab of S; h stays in L2
+  if (colbits) {   // K: the kept row tiles of this 128-column tile's vocabulary tile, 2 k-blocks each
+    const int n_mt = (int)cdiv(mc, kBM);
+    c.kbits = colbits, c.kwords = ld_col, c.list_shift = 1, c.kg_shift = 1;
+    c.ngroups = n_mt, c.clip = n_mt * 2 - c.kblocks;
+  }
+  return c;
+}
+
+// dh[m0 + ..] (+)= S W[v0 + ..]: row tiles of S against W, K = the block's vocabulary columns
+GemmClassH dh_class(int64_t vc, int64_t m0, int64_t mc, int64_t M, int64_t d, bool reduce, int64_t w_k_base,
+                    const uint32_t* rowbits, int ld_row) {
+  GemmClassH c{};
+  c.a_map = 0, c.a_mn = 0, c.a_mn_base = 0, c.a_k_base = 0;
+  c.b_map = 1, c.b_mn = d % 64 == 0 ? 2 : 1, c.b_mn_base = 0, c.b_k_base = (int)w_k_base;
+  c.out_map = 4, c.out_row_base = (int)m0, c.out_col_base = 0;
+  c.reduce = reduce ? 1 : 0;  // the first vocabulary block stores, later ones add
+  c.out_rows = (int)M, c.out_cols = (int)d;
+  c.n_mt = (int)cdiv(mc, kBM), c.n_nt = (int)cdiv(d, kBN), c.kblocks = (int)cdiv(vc, 64);
+  c.mt_major = 1;
+  if (rowbits) {  // K: the kept vocabulary tiles of this row tile, 4 k-blocks each
+    const int n_vt = (int)cdiv(vc, kBN);
+    c.kbits = rowbits, c.kwords = ld_row, c.list_shift = 0, c.kg_shift = 2;
+    c.ngroups = n_vt, c.clip = n_vt * 4 - c.kblocks;
+  }
+  return c;
+}
+
 int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* targets, const uint8_t* mask,
                   const float* lse, const float* g, const float* bmax, float eps, int64_t M, int64_t V, int64_t d,
                   float softcap, float* dh, float* dW, int accumulate_dW, void* workspace, size_t ws_bytes,
@@ -370,7 +411,6 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   R.softcap = softcap > 0.f ? softcap : 0.f;
   R.status = status;
   R.kblocks = (int)cdiv(d, 64);
-  const int n_nt = (int)cdiv(d, kBN);
 
   int64_t block = 0;  // v-block major, m-block minor
   for (int64_t v0 = 0, vblock = 0; v0 < V; v0 += B.Vc, ++vblock) {
@@ -412,32 +452,10 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
       ++block;
       if (launch_recompute(R, st) != cudaSuccess) return ORPO_ERR_CUDA;
 
-      GemmClassH cdw{};  // dW[v0 + ..] (+)= S^T h[m0 + ..]
-      if (dW) {
-        cdw.a_map = 2, cdw.a_mn = 2, cdw.a_mn_base = 0, cdw.a_k_base = 0;
-        cdw.b_map = 3, cdw.b_mn = d64 ? 2 : 1, cdw.b_mn_base = 0, cdw.b_k_base = (int)m0;
-        cdw.out_map = 5, cdw.out_row_base = (int)v0, cdw.out_col_base = 0;
-        cdw.reduce = (m0 > 0 || accumulate_dW) ? 1 : 0;
-        cdw.out_rows = (int)V, cdw.out_cols = (int)d;
-        cdw.n_mt = (int)cdiv(vc, kBM), cdw.n_nt = n_nt, cdw.kblocks = (int)cdiv(mc, 64);
-        cdw.mt_major = 1;  // CTAs running together share one column slab of S; h stays in L2
-        if (skip) {        // K: the kept row tiles of this 128-column tile's vocabulary tile, 2 k-blocks each
-          cdw.kbits = colbits, cdw.kwords = P.shape.ld_col, cdw.list_shift = 1, cdw.kg_shift = 1;
-          cdw.ngroups = n_mt, cdw.clip = n_mt * 2 - cdw.kblocks;
-        }
-      }
-      GemmClassH cdh{};  // dh[m0 + ..] (+)= S W[v0 + ..]
-      cdh.a_map = 0, cdh.a_mn = 0, cdh.a_mn_base = 0, cdh.a_k_base = 0;
-      cdh.b_map = 1, cdh.b_mn = d64 ? 2 : 1, cdh.b_mn_base = 0, cdh.b_k_base = q ? 0 : (int)v0;
-      cdh.out_map = 4, cdh.out_row_base = (int)m0, cdh.out_col_base = 0;
-      cdh.reduce = vblock > 0 ? 1 : 0;
-      cdh.out_rows = (int)M, cdh.out_cols = (int)d;
-      cdh.n_mt = n_mt, cdh.n_nt = n_nt, cdh.kblocks = (int)cdiv(vc, 64);
-      cdh.mt_major = 1;
-      if (skip) {  // K: the kept vocabulary tiles of this row tile, 4 k-blocks each
-        cdh.kbits = rowbits, cdh.kwords = P.shape.ld_row, cdh.list_shift = 0, cdh.kg_shift = 2;
-        cdh.ngroups = n_vt, cdh.clip = n_vt * 4 - cdh.kblocks;
-      }
+      const GemmClassH cdw =
+          dW ? dw_class(v0, vc, m0, mc, V, d, accumulate_dW, skip ? colbits : nullptr, P.shape.ld_col) : GemmClassH{};
+      const GemmClassH cdh =
+          dh_class(vc, m0, mc, M, d, vblock > 0, q ? 0 : v0, skip ? rowbits : nullptr, P.shape.ld_row);
       // longer tiles first
       if (dW && cdw.kblocks >= cdh.kblocks) {
         G.cls[0] = cdw;
