@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 namespace {
 template <int cap, bool kFilter>
 cudaError_t launch_rec_kernel(const RecLaunch& L, cudaStream_t st) {
-  static int smem_set[64] = {0};
+  static std::atomic<int> smem_set[64];
   if (cudaError_t e = opt_in_smem(rec_kernel<cap, kFilter>, SMEM_TOTAL, smem_set)) return e;
   const int chunk = L.chunk > 0 && L.chunk < L.n_mt ? L.chunk : L.n_mt;
   RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks, L.w_row0, L.list, L.count, chunk};
@@ -432,7 +432,7 @@ cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st) {
 }
 
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
-  static int smem_set[64] = {0};
+  static std::atomic<int> smem_set[64];
   if (cudaError_t e = opt_in_smem(gemm_kernel, SMEM_TOTAL, smem_set)) return e;
   GemmSched sched;
   for (int i = 0; i < 6; ++i) sched.maps[i] = nullptr;

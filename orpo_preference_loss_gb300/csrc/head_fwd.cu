@@ -251,7 +251,7 @@ __global__ void merge_kernel(const float* __restrict__ part_m, const float* __re
 
 template <int cap, bool kPair>
 cudaError_t launch_fwd_kernel(const FwdLaunch& L, cudaStream_t st) {
-  static int smem_set[64] = {0};
+  static std::atomic<int> smem_set[64];
   if (cudaError_t e = opt_in_smem(fwd_kernel<cap, kPair>, SMEM_TOTAL, smem_set)) return e;
   const int n_mt = kPair ? (L.n_mt + 1) & ~1 : L.n_mt;
   const int n_mu = kPair ? n_mt / 2 : n_mt;
@@ -293,11 +293,12 @@ cudaError_t launch_fwd_cap(const FwdLaunch& L, cudaStream_t st) {
 }  // namespace
 
 int forward_pair_clusters() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];  // 0 unknown, -1 unavailable, else the cluster count
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] != 0) return cached[dev] > 0 ? cached[dev] : 0;
-  static int smem_set[64] = {0};
+  const int c = cached[dev].load(std::memory_order_acquire);
+  if (c != 0) return c > 0 ? c : 0;
+  static std::atomic<int> smem_set[64];
   int n = 0;
   if (opt_in_smem(fwd_kernel<kCapExp, true>, SMEM_TOTAL, smem_set) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
@@ -314,7 +315,7 @@ int forward_pair_clusters() {
     if (cudaOccupancyMaxActiveClusters(&n, fwd_kernel<kCapExp, true>, &cfg) != cudaSuccess) n = 0;
   }
   cudaGetLastError();
-  cached[dev] = n > 0 ? n : -1;
+  cached[dev].store(n > 0 ? n : -1, std::memory_order_release);
   return n > 0 ? n : 0;
 }
 

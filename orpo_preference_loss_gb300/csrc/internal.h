@@ -5,17 +5,20 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace orpo {
 
 // ---- kernels using more than 48 KiB of dynamic shared memory opt in once per device
-// (`done` is the caller's per-kernel table of devices already set)
+// (`done` is the caller's per-kernel table of devices already set; host threads may race to set
+// it, which only repeats an idempotent attribute call)
 template <class Kernel>
-inline cudaError_t opt_in_smem(Kernel kernel, int bytes, int (&done)[64]) {
+inline cudaError_t opt_in_smem(Kernel kernel, int bytes, std::atomic<int> (&done)[64]) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  if (dev < 0 || dev >= 64 || done[dev]) return cudaSuccess;
+  if (dev < 0 || dev >= 64 || done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done[dev] = 1;
+  if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
   return e;
 }
 

@@ -340,15 +340,9 @@ cudaError_t launch_loss(int kind, const float* logp, const int32_t* seq_id, cons
                         float beta, float gamma, const float* ref, float* out, float* ell, float* g, int32_t* status,
                         cudaStream_t st) {
   const size_t smem = loss_smem_bytes(P);
-  // raise the kernel's dynamic shared-memory limit only when a larger size than before is needed
-  static int limit[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || (int)smem > limit[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(loss_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) limit[dev] = (int)smem;
-  }
+  // one opt-in per device, at the size of the largest accepted batch (ORPO_MAX_PAIRS pairs)
+  static std::atomic<int> smem_set[64];
+  if (cudaError_t e = opt_in_smem(loss_kernel, (int)loss_smem_bytes(ORPO_MAX_PAIRS), smem_set)) return e;
   prof_begin(K_LOSS, st);
   loss_kernel<<<1, T, smem, st>>>(kind, logp, seq_id, mask, M, P, beta, gamma, ref, out, ell, g, status);
   prof_end(K_LOSS, st);
