@@ -72,7 +72,8 @@ def test_block_max_matches_oracle(name, M, V, d, softcap):
 # recipe uncapped, 1 - p(target) falls to ~2e-5 and the fp32 logits' rounding alone moves the target
 # coefficient g (1 - p) by several percent, filter or not.
 @pytest.mark.parametrize("name,M,V,d,softcap,eps", [("e4b_sharp", 512, 65536, 256, 30.0, 1e-5),
-                                                    ("e4b", 512, 65536, 256, 0.0, 3e-3)])
+                                                    ("e4b", 512, 65536, 256, 0.0, 3e-3),
+                                                    ("e4b", 512, 65536, 256, 1000.0, 3e-3)])  # hybrid softcap form
 def test_skip_matches_filtered_oracle(name, M, V, d, softcap, eps):
     w = workloads.make(name, M=M, d=d, V=V)
     h, W = f64(w.h), f64(w.W)
