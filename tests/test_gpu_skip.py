@@ -232,3 +232,41 @@ def test_quantised_head_with_skips():
     rdh, rdW = oracle.head_backward(h, Wd, w.targets, w.mask, lse32, g, softcap, filter_eps=eps)
     assert relfro(grads[0][0], rdh) < GRAD_RELFRO and relfro(grads[0][1], rdW) < GRAD_RELFRO
     assert np.array_equal(grads[0][0], grads[1][0]) and np.array_equal(grads[0][1], grads[1][1])
+
+
+def test_quantised_skips_are_the_bf16_skips_on_the_dequantised_weights():
+    # several dequantised blocks (2 forward W blocks of 131072 rows, 32 backward vocabulary blocks):
+    # the quantised path computes the same tiles in the same order as the bf16 path fed the
+    # dequantised weights, so the block maxima and the skipped backward agree bit for bit
+    w = workloads.make("e4b_sharp", M=16384, d=1024, V=262144)
+    bits, group, softcap, eps = 4, 64, 30.0, 1e-5
+    wq, s, b = workloads.quantize_affine(w.W, bits, group)
+    Wd = oracle.dequant_affine(wq, s, b, bits, group, w.d)
+    M, V, d = w.M, w.V, w.d
+    t = to_dev(w)
+    t["W"] = torch.from_numpy(workloads.round_bf16(Wd.astype(np.float32)).view(np.int16)).to(dev()).view(torch.bfloat16)
+    q = (torch.from_numpy(wq).to(dev()), torch.from_numpy(s.view(np.int16)).to(dev()).view(torch.bfloat16),
+         torch.from_numpy(b.view(np.int16)).to(dev()).view(torch.bfloat16))
+    assert orpo.orpo_head_q_workspace_bytes(M, V, d) < V * d * 2 + orpo.orpo_head_workspace_bytes(M, V, d)
+    wsq = torch.empty(orpo.orpo_head_q_workspace_bytes(M, V, d), dtype=torch.uint8, device=dev())
+    st = status_tensor()
+    lse_q = torch.empty(M, device=dev())
+    logp_q = torch.empty(M, device=dev())
+    bm_q = torch.full(orpo.block_max_shape(M, V), float("nan"), device=dev())
+    orpo.orpo_head_fwd_q_bmax(t["h"], *q, bits, group, t["targets"], t["mask"], softcap, logp_q, lse_q, bm_q, wsq, st)
+    logp_b, lse_b, bm_b, st_b = fwd_bmax(t, M, V, d, softcap)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and st_b == 0
+    assert np.array_equal(bm_q.cpu().numpy(), bm_b.cpu().numpy())
+    assert np.max(np.abs(lse_q.cpu().numpy() - lse_b)) < 1e-4     # only the split merge order differs
+    g = orpo_g(w, logp_b.astype(np.float64)).astype(np.float32)
+    lse_t = torch.from_numpy(lse_b).to(dev())
+    g_t = torch.from_numpy(g).to(dev())
+    dh_q = torch.empty((M, d), device=dev())
+    dW_q = torch.empty((V, d), device=dev())
+    orpo.orpo_head_bwd_q_skip(t["h"], *q, bits, group, t["targets"], t["mask"], lse_t, g_t, bm_q, eps, softcap, dh_q,
+                              dW_q, False, wsq, st)
+    dh_b, dW_b, st_b = bwd_skip(t, lse_b, g, bm_b, eps, M, V, d, softcap)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and st_b == 0
+    assert np.array_equal(dh_q.cpu().numpy(), dh_b) and np.array_equal(dW_q.cpu().numpy(), dW_b)
