@@ -84,3 +84,18 @@ def test_bitwise_reproducible():
     a = run(logp, w.seq_id, w.mask, w.n_pairs, w.lam)
     b = run(logp, w.seq_id, w.mask, w.n_pairs, w.lam)
     assert all(np.array_equal(x, y) for x, y in zip(a[:3], b[:3]))
+
+
+def test_largest_pair_count():
+    # ORPO_MAX_PAIRS pairs: the loss kernel's largest shared-memory layout
+    import orpo_preference_loss_gb300 as orpo
+    P = orpo.MAX_PAIRS
+    rng = np.random.default_rng(11)
+    lengths = rng.integers(1, 9, size=2 * P)
+    seq = np.repeat(np.arange(2 * P), lengths).astype(np.int32)
+    mask = np.ones(len(seq), dtype=np.uint8)
+    logp = workloads.synthetic_logp(13, seq, mask, scale=1.0, offset=-0.5)
+    compare(logp, seq, mask, P, 0.1)
+    # and a small batch right after it on the same device still runs (the opt-in covers every size)
+    seq2 = np.repeat(np.arange(4), 3).astype(np.int32)
+    compare(workloads.synthetic_logp(14, seq2, np.ones(12, np.uint8)), seq2, np.ones(12, np.uint8), 2, 0.1)
