@@ -97,7 +97,7 @@ size_t orpo_head_workspace_bytes(int64_t M, int64_t V, int64_t d);
  * targets: int32 [M]; mask: uint8 [M] (nonzero = response row).
  * Device errors: ORPO_STATUS_TARGET (logp[t] is then 0),
  * ORPO_STATUS_NONFINITE (an lse that is not finite).
- * M = 0 is a no-op.  Limits: 1 <= V < 2^31, 8 <= d < 2^20, M < 2^31.
+ * M = 0 is a no-op.  Limits: 1 <= V <= 2^31 - 2^16, 8 <= d < 2^20, M <= 2^31 - 2^16.
  */
 int orpo_head_fwd(const void* h_bf16, const void* W_bf16, const int32_t* targets,
                   const uint8_t* mask, int64_t M, int64_t V, int64_t d, float softcap,
@@ -124,7 +124,7 @@ int orpo_head_fwd(const void* h_bf16, const void* W_bf16, const int32_t* targets
  * transcendentals are evaluated in fp32 on fp64-formed arguments.
  * Device errors: ORPO_STATUS_SEQID, ORPO_STATUS_EMPTY_SEQ, ORPO_STATUS_NONFINITE
  * (e.g. l = 0 makes log1mexp -inf; it is reported, not clamped).
- * Limits: 1 <= n_pairs <= ORPO_MAX_PAIRS, 0 <= M < 2^31, lambda >= 0.
+ * Limits: 1 <= n_pairs <= ORPO_MAX_PAIRS, 0 <= M <= 2^31 - 2^16, lambda >= 0.
  */
 int orpo_loss(const float* logp, const int32_t* seq_id, const uint8_t* mask, int64_t M,
               int32_t n_pairs, float lambda, float* out, float* ell, float* g,

@@ -16,7 +16,9 @@ size_t loss_smem_bytes(int P);
 
 namespace {
 
-constexpr int64_t kMaxRows = (1ll << 31) - 1;
+// Largest M, V (and debug-GEMM extent): row and column indices, tile counts rounded up to whole tiles,
+// and per-thread row chunks of the loss stay inside int32 with room to spare.
+constexpr int64_t kMaxRows = (1ll << 31) - (1ll << 16);
 
 // ---------------------------------------------------------------- driver entry point
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;

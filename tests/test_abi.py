@@ -48,6 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 FAKE = ctypes.c_void_p(0x10000)       # never dereferenced: every case fails before any CUDA call
 MISALIGNED = ctypes.c_void_p(0x10008)
+MAX_ROWS = (1 << 31) - (1 << 16)   # largest M and V the header documents
 
 
 def fwd(lib, h=FAKE, W=FAKE, M=64, V=128, d=64, softcap=0.0, ws_bytes=1 << 30, tgt=FAKE, ws=FAKE):
@@ -66,6 +67,8 @@ def test_forward_host_checks(lib):
     assert fwd(lib, softcap=math.inf) == ERR_ARG
     assert fwd(lib, ws_bytes=16) == ERR_WS
     assert fwd(lib, M=0) == OK              # empty input: nothing to launch
+    assert fwd(lib, M=MAX_ROWS + 1) == ERR_SHAPE
+    assert fwd(lib, V=MAX_ROWS + 1) == ERR_SHAPE
 
 
 def test_loss_host_checks(lib):
@@ -74,6 +77,7 @@ def test_loss_host_checks(lib):
     assert call(P=0) == ERR_SHAPE
     assert call(P=orpo.MAX_PAIRS + 1) == ERR_SHAPE
     assert call(M=-3) == ERR_SHAPE
+    assert call(M=MAX_ROWS + 1) == ERR_SHAPE
     assert call(logp=None) == ERR_NULL
     assert call(lam=-0.1) == ERR_ARG
     assert call(lam=math.nan) == ERR_ARG
@@ -107,6 +111,11 @@ def test_workspace_is_flat_in_M(lib):
     # far below any [M, V] buffer: 8192 x 262144 fp32 logits would be 8 GiB
     assert lib.orpo_head_workspace_bytes(8192, V, d) < (8192 * V * 4) // 16
     assert lib.orpo_head_workspace_bytes(-1, V, d) == 0
+    # the documented limits: M, V <= 2^31 - 2^16
+    assert lib.orpo_head_workspace_bytes(MAX_ROWS, V, d) > 0
+    assert lib.orpo_head_workspace_bytes(8192, MAX_ROWS, 64) > 0
+    assert lib.orpo_head_workspace_bytes(MAX_ROWS + 1, V, d) == 0
+    assert lib.orpo_head_workspace_bytes(8192, MAX_ROWS + 1, 64) == 0
 
 
 def test_skip_host_checks(lib):
