@@ -71,3 +71,31 @@ def test_deterministic():
     a = gpu_forward(t, w.M, w.V, w.d, 0.0)
     b = gpu_forward(t, w.M, w.V, w.d, 0.0)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_rows_agree_whatever_the_batch_around_them():
+    # The same 128 rows alone (one row tile: many vocabulary splits), at the front of an 8192-row
+    # batch (64 row tiles in pairs: few splits) and at its ragged end: the split count, the pairing,
+    # the unit order and the rows' tile position all change, and only the fp32 merge order differs.
+    w = workloads.make("e4b", M=8192, d=256, V=65536 + 320)
+    t = to_dev(w)
+    sub = slice(0, 128)
+
+    def rows_of(idx):
+        u = {k: (v if k == "W" else v[idx].contiguous()) for k, v in t.items()}
+        M = u["targets"].shape[0]
+        return gpu_forward(u, M, w.V, w.d, w.softcap)
+
+    perm = torch.cat([torch.arange(128, 8192 - 5, device=t["h"].device), torch.arange(0, 128, device=t["h"].device),
+                      torch.arange(8192 - 5, 8192, device=t["h"].device)])
+    alone = rows_of(torch.arange(0, 128, device=t["h"].device))
+    front = rows_of(torch.arange(0, 8192, device=t["h"].device))
+    back = rows_of(perm)          # the 128 rows sit at 8059..8186, across a tile boundary
+    assert alone[2] == front[2] == back[2] == 0
+    pos = slice(8192 - 5 - 128, 8192 - 5)
+    for got in ((front[0][sub], front[1][sub]), (back[0][pos], back[1][pos])):
+        assert np.max(np.abs(got[0] - alone[0])) < 1e-4
+        assert np.max(np.abs(got[1] - alone[1])) < 1e-4
+    rl, rs = oracle.head_forward(f64(w.h[sub]), f64(w.W), w.targets[sub], w.mask[sub], w.softcap)
+    assert np.max(np.abs(alone[1] - rs)) < LOGP_ATOL
+    assert np.max(np.abs(alone[0] - rl)) < LOGP_ATOL
