@@ -69,7 +69,9 @@ enum {
   ORPO_STATUS_SEQID = 1 << 5,      /* seq_id outside [-1, 2P) or ids not non-decreasing */
   ORPO_STATUS_EMPTY_SEQ = 1 << 6,  /* a sequence has no mask = 1 row (its mean is undefined) */
   ORPO_STATUS_NONFINITE = 1 << 7,  /* a non-finite lse, loss, log-odds or gradient */
-  ORPO_STATUS_TIMEOUT = 1 << 8     /* a bounded on-chip wait gave up (the kernel returned early) */
+  ORPO_STATUS_TIMEOUT = 1 << 8,    /* a bounded on-chip wait gave up (the kernel returned early) */
+  ORPO_STATUS_BOUNDS = 1 << 9      /* bounds-checked build only (ORPO_DEBUG_BOUNDS): a computed index fell
+                                      outside its buffer; the access was skipped */
 };
 
 /* Largest number of pairs orpo_loss accepts. */

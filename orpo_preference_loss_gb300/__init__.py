@@ -21,9 +21,11 @@ __all__ = [
     "orpo_head_bwd", "orpo_status_string", "orpo_debug_gemm", "OrpoHead", "STATUS_BITS",
     "orpo_profile_start", "orpo_profile_stop", "orpo_head_fwd_static", "orpo_debug_wait_timeout",
     "orpo_pref_loss", "PREF_KINDS", "orpo_head_q_workspace_bytes", "orpo_head_fwd_q", "orpo_head_bwd_q",
+    "use_bounds_checked_library",
 ]
 
-STATUS_BITS = {"target": 1 << 4, "seqid": 1 << 5, "empty": 1 << 6, "nonfinite": 1 << 7, "timeout": 1 << 8}
+STATUS_BITS = {"target": 1 << 4, "seqid": 1 << 5, "empty": 1 << 6, "nonfinite": 1 << 7, "timeout": 1 << 8,
+               "bounds": 1 << 9}
 MAX_PAIRS = 2048
 
 _lib = None
@@ -35,16 +37,30 @@ class OrpoError(RuntimeError):
         self.code = code
 
 
+_variant = "release"
+
+
 def lib_path() -> str:
-    return _build.LIB_PATH
+    return _build.DEBUG_LIB_PATH if _variant == "debug" else _build.LIB_PATH
+
+
+def use_bounds_checked_library() -> None:
+    """Bind this process to liborpo_head_debug.so (build(debug=True)) instead of liborpo_head.so.
+
+    The bounds-checked build checks every computed index against its buffer and reports a miss
+    as ORPO_STATUS_BOUNDS; its arithmetic is the release build's.  Call before the first use."""
+    global _variant
+    if _lib is not None and _variant != "debug":
+        raise RuntimeError("the release library is already loaded in this process")
+    _variant = "debug"
 
 
 def load():
-    """Load liborpo_head.so (built in-tree); raises if it is missing."""
+    """Load the library (built in-tree); raises if it is missing."""
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.LIB_PATH
+    path = lib_path()
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with orpo_preference_loss_gb300.build.build()")
     L = ctypes.CDLL(path)

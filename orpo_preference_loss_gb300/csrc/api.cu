@@ -259,6 +259,7 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   L.lse = lse;
   L.part_m = base;
   L.part_s = base + (size_t)nsplit_max * Mpad;
+  L.part_cap = nsplit_max;
   L.M = (int)M;
   L.Mpad = (int)Mpad;
   L.V = (int)V;
@@ -279,7 +280,7 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
     const int64_t vc = std::min(vb, V - v0);
     const int64_t n_vt = cdiv(vc, kBN);
     if (q) {
-      if (launch_dequant(q->wq, q->scales, q->biases, q->bits, q->group, v0, vc, d, Wb, st) != cudaSuccess)
+      if (launch_dequant(q->wq, q->scales, q->biases, q->bits, q->group, v0, vc, d, V, Wb, status, st) != cudaSuccess)
         return ORPO_ERR_CUDA;
       if (!encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Wb, d, vc, d * 2, 64, w_box)) return ORPO_ERR_CUDA;
     } else if (!encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, w_box)) {
@@ -314,6 +315,7 @@ GemmClassH dw_class(int64_t v0, int64_t vc, int64_t m0, int64_t mc, int64_t V, i
     const int n_mt = (int)cdiv(mc, kBM);
     c.kbits = colbits, c.kwords = ld_col, c.list_shift = 1, c.kg_shift = 1;
     c.ngroups = n_mt, c.clip = n_mt * 2 - c.kblocks;
+    c.kbits_rows = (int)cdiv(vc, kBN);
   }
   return c;
 }
@@ -333,6 +335,7 @@ GemmClassH dh_class(int64_t vc, int64_t m0, int64_t mc, int64_t M, int64_t d, bo
     const int n_vt = (int)cdiv(vc, kBN);
     c.kbits = rowbits, c.kwords = ld_row, c.list_shift = 0, c.kg_shift = 2;
     c.ngroups = n_vt, c.clip = n_vt * 4 - c.kblocks;
+    c.kbits_rows = (int)cdiv(mc, kBM);
   }
   return c;
 }
@@ -374,6 +377,7 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
     P.Mc = B.Mc, P.Vc = B.Vc, P.n_mblocks = (int)n_mblocks;
     P.shape = skip_shape(B);
     P.area = reinterpret_cast<uint8_t*>(counters + kCounters);
+    P.area_bytes = kSkipBytes;
     P.thr2 = log2f(eps);
     P.chunk_bytes = (int64_t)kBM * d * 2;
     if ((int64_t)P.shape.n_mt * P.shape.n_vt > kMaxTiles) return ORPO_ERR_SHAPE;  // cannot happen: Mc Vc bounded
@@ -418,7 +422,7 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   for (int64_t v0 = 0, vblock = 0; v0 < V; v0 += B.Vc, ++vblock) {
     const int64_t vc = std::min(B.Vc, V - v0);
     if (q) {
-      if (launch_dequant(q->wq, q->scales, q->biases, q->bits, q->group, v0, vc, d, Wb, st) != cudaSuccess ||
+      if (launch_dequant(q->wq, q->scales, q->biases, q->bits, q->group, v0, vc, d, V, Wb, status, st) != cudaSuccess ||
           !encode_w(Wb, vc))
         return ORPO_ERR_CUDA;
     }
@@ -658,7 +662,8 @@ const char* orpo_status_string(int code) {
               {ORPO_STATUS_SEQID, "bad sequence id"},
               {ORPO_STATUS_EMPTY_SEQ, "empty sequence"},
               {ORPO_STATUS_NONFINITE, "non-finite value"},
-              {ORPO_STATUS_TIMEOUT, "on-chip wait timed out"}};
+              {ORPO_STATUS_TIMEOUT, "on-chip wait timed out"},
+              {ORPO_STATUS_BOUNDS, "index out of bounds (bounds-checked build)"}};
   for (const auto& b : bits) {
     if (code & b.bit) {
       if (buf[0]) strncat(buf, "; ", sizeof(buf) - strlen(buf) - 1);
@@ -737,6 +742,7 @@ extern "C" int orpo_head_fwd_static(const void* h, const void* W, const int32_t*
   L.lse = lse;
   L.part_m = part;
   L.part_s = part + (size_t)L.nsplit * Mpad;
+  L.part_cap = L.nsplit;
   L.M = (int)M;
   L.Mpad = (int)Mpad;
   L.V = (int)V;

@@ -22,6 +22,7 @@
 #pragma once
 
 #include "../../include/orpo_head.h"
+#include "bounds.cuh"
 #include "ptx.cuh"
 
 namespace orpo {

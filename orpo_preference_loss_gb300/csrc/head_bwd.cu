@@ -29,12 +29,18 @@ struct RecSched {
   const int* list;   // backward skips: the tiles to compute (vt * n_mt + mt, in unit order), or nullptr
   const int* count;  // number of entries of list
   int chunk;         // row tiles per L2 chunk (chunk_decode)
+  int32_t* status = nullptr;
   __device__ int num_units() const { return list ? __ldg(count) : n_mt * n_vt; }
   __device__ int tile_index(int u) const {
-    if (list) return __ldg(list + u);
-    int mt, vt;
-    chunk_decode(u, n_mt, n_vt, chunk, mt, vt);
-    return vt * n_mt + mt;
+    int x;
+    if (list) {
+      x = in_bounds(status, u, kMaxTiles) ? __ldg(list + u) : 0;
+    } else {
+      int mt, vt;
+      chunk_decode(u, n_mt, n_vt, chunk, mt, vt);
+      x = vt * n_mt + mt;
+    }
+    return in_bounds(status, x, n_mt * n_vt) ? x : 0;
   }
   __device__ int unit_len(int) const { return 1; }
   __device__ TileOps tile(int u, int) const {
@@ -148,6 +154,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                const __grid_constant__ CUtensorMap ms, RecSched sched, RecArgs p) {
   sched.mh = &mh;
   sched.mw = &mw;
+  sched.status = p.status;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&mh);
     tma_prefetch_desc(&mw);
@@ -216,8 +223,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if constexpr (kFilter) {
         const bool keep = gval != 0.f && amax >= p.eps * fabsf(gval);
         if (__any_sync(0xffffffffu, keep) && lane == 0) {
-          atomicOr(p.rowbits + mt * p.ld_row + (vt >> 5), 1u << (vt & 31));
-          atomicOr(p.colbits + vt * p.ld_col + (mt >> 5), 1u << (mt & 31));
+          if (in_bounds(p.status, mt, sched.n_mt) && in_bounds(p.status, vt >> 5, p.ld_row))
+            atomicOr(p.rowbits + mt * p.ld_row + (vt >> 5), 1u << (vt & 31));
+          if (in_bounds(p.status, vt, sched.n_vt) && in_bounds(p.status, mt >> 5, p.ld_col))
+            atomicOr(p.colbits + vt * p.ld_col + (mt >> 5), 1u << (mt & 31));
         }
       }
     }
@@ -239,11 +248,13 @@ struct GemmClass {
   // (past the operands' K extent).  kbits == nullptr: dense, kblocks.
   const uint32_t* kbits;
   int kwords, list_shift, kg_shift, ngroups, clip;
+  int kbits_rows;  // bitmaps at kbits
 };
 
 struct GemmSched {
   const CUtensorMap* maps[6];
   GemmClass cls[2];
+  int32_t* status;
   // constant-index selection keeps the pointer table in registers (no local-memory copy)
   __device__ __forceinline__ const CUtensorMap* map(int i) const {
     switch (i) {
@@ -288,7 +299,8 @@ struct GemmSched {
     t.b = Operand{map(c.b_map), c.b_mn, c.b_mn_base + nt * BN, c.b_k_base};
     t.kblocks = c.kblocks;
     if (c.kbits != nullptr) {
-      const uint32_t* bits = c.kbits + (size_t)(mt >> c.list_shift) * c.kwords;
+      const int br = in_bounds(status, mt >> c.list_shift, c.kbits_rows) ? mt >> c.list_shift : 0;
+      const uint32_t* bits = c.kbits + (size_t)br * c.kwords;
       int n = 0;
       for (int w = 0; w < c.kwords; ++w) n += __popc(__ldg(bits + w));
       const int lg = c.ngroups - 1;
@@ -313,6 +325,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   sched.maps[3] = &m3;
   sched.maps[4] = &m4;
   sched.maps[5] = &m5;
+  sched.status = status;
   if (threadIdx.x == 0) {
     for (int i = 0; i < 6; ++i) tma_prefetch_desc(sched.maps[i]);
   }
@@ -436,12 +449,14 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
   if (cudaError_t e = opt_in_smem(gemm_kernel, SMEM_TOTAL, smem_set)) return e;
   GemmSched sched;
   for (int i = 0; i < 6; ++i) sched.maps[i] = nullptr;
+  sched.status = nullptr;
   for (int k = 0; k < 2; ++k) {
     const GemmClassH& h = L.cls[k];
     sched.cls[k] = GemmClass{h.a_map,     h.a_mn,      h.a_mn_base,  h.a_k_base,     h.b_map,        h.b_mn,
                              h.b_mn_base, h.b_k_base,  h.out_map,    h.out_row_base, h.out_col_base, h.reduce,
                              h.out_rows,  h.out_cols,  h.n_mt,       h.n_nt,         h.kblocks,      h.mt_major,
-                             h.kbits,     h.kwords,    h.list_shift, h.kg_shift,     h.ngroups,      h.clip};
+                             h.kbits,     h.kwords,    h.list_shift, h.kg_shift,     h.ngroups,      h.clip,
+                             h.kbits_rows};
   }
   prof_begin(kind, st);
   gemm_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.maps[0], L.maps[1], L.maps[2], L.maps[3], L.maps[4],

@@ -72,6 +72,7 @@ struct FwdArgs {
   float* bmax;   // optional block maxima [ceil(M/32), bmax_ld]: max of x over a 32-row group's mask != 0
                  // rows and one 256-column vocabulary tile (-inf for a group with no such row)
   int bmax_ld;   // ceil(V / 256)
+  int part_cap;  // splits the partial arrays hold (each Mpad floats)
 };
 
 // Per-row online softmax state of one epilogue thread, base-2 units.
@@ -211,11 +212,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           float v = supervised ? tmax : -INFINITY;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-          if (lane == 0 && grp * 32 < p.M) p.bmax[(size_t)grp * p.bmax_ld + col_base / BN] = v;
+          if (lane == 0 && grp * 32 < p.M && in_bounds(p.status, col_base / BN, p.bmax_ld))
+            p.bmax[(size_t)grp * p.bmax_ld + col_base / BN] = v;
         }
       }
-      if (row < p.Mpad) {  // pair mode pads an odd tile count with one empty tile
-        p.part_m[(size_t)(p.split0 + s) * p.Mpad + row] = st.m;
+      if (row < p.Mpad && in_bounds(p.status, p.split0 + s, p.part_cap)) {  // pair mode pads an odd
+        p.part_m[(size_t)(p.split0 + s) * p.Mpad + row] = st.m;                // tile count with an empty tile
         p.part_s[(size_t)(p.split0 + s) * p.Mpad + row] = st.s;
       }
     }
@@ -228,7 +230,7 @@ __global__ void merge_kernel(const float* __restrict__ part_m, const float* __re
                              const uint8_t* __restrict__ mask, float* __restrict__ logp, float* __restrict__ lse,
                              int32_t* status) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= M) return;
+  if (t >= M || !in_bounds(status, t, Mpad)) return;
   float gm = -INFINITY;
   for (int k = 0; k < nsplit; ++k) gm = fmaxf(gm, part_m[(size_t)k * Mpad + t]);
   float S = 0.f;
@@ -258,7 +260,7 @@ cudaError_t launch_fwd_kernel(const FwdLaunch& L, cudaStream_t st) {
   const int chunk = L.chunk > 0 && L.chunk < n_mu ? L.chunk : n_mu;
   FwdSched sched{nullptr, nullptr, n_mt, L.nsplit, L.n_vt, L.kblocks, chunk, 0, 0};
   FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M,      L.Mpad,
-            L.V,       L.softcap, L.status, L.col0, L.split0, L.bmax, (L.V + BN - 1) / BN};
+            L.V,       L.softcap, L.status, L.col0, L.split0, L.bmax, (L.V + BN - 1) / BN, L.part_cap};
   cudaError_t e = cudaSuccess;
   prof_begin(K_FWD, st);
   if constexpr (kPair) {

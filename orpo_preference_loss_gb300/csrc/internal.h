@@ -62,6 +62,7 @@ struct FwdLaunch {
   int grid;
   int col0 = 0;    // vocabulary column of row 0 of mw
   int split0 = 0;  // first split index this launch writes
+  int part_cap = 0;  // splits part_m / part_s hold (Mpad floats each)
   int pair = 0;    // 1: 2-CTA clusters share W tiles (mw box {64,128}; grid = 2 x clusters; n_mt padded to even)
   float* bmax = nullptr;  // optional block maxima [ceil(M/32), ceil(V/256)] (base-2 softcapped logits)
   int chunk = 0;          // M units per L2 chunk (l2_chunk); 0: all of them
@@ -122,6 +123,7 @@ struct SkipPlan {
   int first_block, nblocks;  // this round: blocks first_block .. first_block + nblocks - 1, slot b - first_block
   SkipShape shape;    // of a full block (edge blocks use a prefix of it)
   uint8_t* area;      // slot s at area + s * shape.slot_bytes
+  size_t area_bytes;
   float thr2;         // log2(eps)
   int32_t* status;
   int64_t chunk_bytes;  // h bytes per row tile: the list follows the recompute's l2_chunk order
@@ -130,7 +132,8 @@ cudaError_t launch_skip_plan(const SkipPlan& P, cudaStream_t st);  // lists and 
 
 // ---- quantised head: affine group dequantisation of W rows [v0, v0 + rows) into bf16 [rows, d]
 cudaError_t launch_dequant(const uint8_t* wq, const void* scales, const void* biases, int bits, int group,
-                           int64_t v0, int64_t rows, int64_t d, void* out_bf16, cudaStream_t st);
+                           int64_t v0, int64_t rows, int64_t d, int64_t V, void* out_bf16, int32_t* status,
+                           cudaStream_t st);
 
 // ---- generic two-class GEMM with an fp32 store / reduce-add epilogue
 struct GemmClassH {
@@ -144,6 +147,7 @@ struct GemmClassH {
   // kbits + index * kwords; ngroups groups, the last clip k-blocks short; nullptr: dense
   const uint32_t* kbits = nullptr;
   int kwords = 0, list_shift = 0, kg_shift = 0, ngroups = 0, clip = 0;
+  int kbits_rows = 0;  // bitmaps at kbits (bounds-checked build)
 };
 struct GemmLaunch {
   CUtensorMap maps[6];

@@ -23,6 +23,7 @@
 #include <math.h>
 
 #include "../../include/orpo_head.h"
+#include "bounds.cuh"
 #include "internal.h"
 
 namespace orpo {
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(T, 1)
         if (cur >= 0) {
           if (nruns == 0) {
             hs = cur, hsum = sum, hc = cnt, hfsum = fsum, hfc = fcnt;
-          } else {
+          } else if (in_bounds(status, cur, S)) {
             seq_sum[cur] = sum;  // a run strictly inside the chunk is the whole sequence
             seq_cnt[cur] = cnt;
             seq_fsum[cur] = fsum;

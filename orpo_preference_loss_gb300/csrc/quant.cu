@@ -15,6 +15,7 @@
 
 #include <algorithm>
 
+#include "bounds.cuh"
 #include "internal.h"
 
 namespace orpo {
@@ -48,7 +49,8 @@ template <int kBits>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ wq,
                                                       const uint16_t* __restrict__ scales,
                                                       const uint16_t* __restrict__ biases, int group, int64_t v0,
-                                                      int rows, int d, uint4* __restrict__ out) {
+                                                      int rows, int d, int64_t V, uint4* __restrict__ out,
+                                                      int32_t* status) {
   const uint32_t per_row = (uint32_t)d / 8u;
   const uint32_t nslices = (uint32_t)rows * per_row;
   const uint32_t ngroups = (uint32_t)(d / group);
@@ -64,6 +66,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
       if (idx < nslices) {
         const uint32_t r = idx / per_row, c = idx - r * per_row;
         const int64_t v = v0 + r;
+        if (!in_bounds(status, v, V)) continue;
         const uint8_t* row = wq + v * (int64_t)(d * kBits / 8);
         if constexpr (kBits == 4)
           raw[k].x = __ldg(reinterpret_cast<const uint32_t*>(row) + c);
@@ -90,7 +93,8 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
 }  // namespace
 
 cudaError_t launch_dequant(const uint8_t* wq, const void* scales, const void* biases, int bits, int group,
-                           int64_t v0, int64_t rows, int64_t d, void* out_bf16, cudaStream_t st) {
+                           int64_t v0, int64_t rows, int64_t d, int64_t V, void* out_bf16, int32_t* status,
+                           cudaStream_t st) {
   const int64_t n = rows * (d / 8);
   if (n >= (1ll << 31)) return cudaErrorInvalidValue;  // cannot happen: a block is bounded by kWBlockBudget
   const int threads = 256;
@@ -100,9 +104,9 @@ cudaError_t launch_dequant(const uint8_t* wq, const void* scales, const void* bi
   uint4* o = static_cast<uint4*>(out_bf16);
   prof_begin(K_DEQUANT, st);
   if (bits == 4)
-    dequant_kernel<4><<<(int)blocks, threads, 0, st>>>(wq, sc, bi, group, v0, (int)rows, (int)d, o);
+    dequant_kernel<4><<<(int)blocks, threads, 0, st>>>(wq, sc, bi, group, v0, (int)rows, (int)d, V, o, status);
   else
-    dequant_kernel<8><<<(int)blocks, threads, 0, st>>>(wq, sc, bi, group, v0, (int)rows, (int)d, o);
+    dequant_kernel<8><<<(int)blocks, threads, 0, st>>>(wq, sc, bi, group, v0, (int)rows, (int)d, V, o, status);
   prof_end(K_DEQUANT, st);
   return cudaGetLastError();
 }

@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const SkipPlan P) {
   const int m0 = (int)(mb * P.Mc), v0 = (int)(vb * P.Vc);
   const int mc = (int)min((int64_t)P.M - m0, P.Mc), vc = (int)min((int64_t)P.V - v0, P.Vc);
   const int n_mt = (mc + 127) / 128, n_vt = (vc + 255) / 256;
+  if (!in_bounds(P.status, (int64_t)(blockIdx.x + 1) * P.shape.slot_bytes - 1, P.area_bytes)) return;
   uint8_t* slot = P.area + (size_t)blockIdx.x * P.shape.slot_bytes;
   uint32_t* bits = reinterpret_cast<uint32_t*>(slot + P.shape.rowbits_off());  // rowbits, then colbits
   const int nwords = P.shape.n_mt * P.shape.ld_row + P.shape.n_vt * P.shape.ld_col;
@@ -56,6 +57,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const SkipPlan P) {
   int* count = reinterpret_cast<int*>(slot + P.shape.count_off());
   const int ntiles = n_mt * n_vt;
   const int ngroups = (mc + 31) / 32;
+  // the shared tables hold a block of at most kMcMax rows and kMaxTiles tiles (uniform over the block)
+  if (!in_bounds(P.status, ntiles - 1, kMaxTiles) || !in_bounds(P.status, ngroups - 1, kGroupsMax)) return;
   for (int i = tid; i < ntiles; i += kPlanThreads) hot[i] = 0;
   __syncthreads();
   // one row per thread: a warp covers one 32-row group per pass
@@ -68,12 +71,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const SkipPlan P) {
       const int y = P.targets[t];
       if (y < 0 || y >= P.V)
         atomicOr(P.status, ORPO_STATUS_TARGET);
-      else if (y >= v0 && y < v0 + vc)
+      else if (y >= v0 && y < v0 + vc && in_bounds(P.status, (r / 128) * n_vt + (y - v0) / 256, kMaxTiles))
         hot[(r / 128) * n_vt + (y - v0) / 256] = 1;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l2 = fminf(l2, __shfl_xor_sync(0xffffffffu, l2, o));
-    if (lane == 0) minlse2[r / 32] = l2;
+    if (lane == 0 && in_bounds(P.status, r / 32, kGroupsMax)) minlse2[r / 32] = l2;
   }
   __syncthreads();
   // each thread judges kPerThread consecutive tiles in the recompute's unit order (chunk_decode),
@@ -87,10 +90,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const SkipPlan P) {
     if (u >= ntiles) continue;
     int mt, vt;
     chunk_decode(u, n_mt, n_vt, chunk, mt, vt);
-    int hit = hot[mt * n_vt + vt];
+    int hit = in_bounds(P.status, mt * n_vt + vt, kMaxTiles) ? hot[mt * n_vt + vt] : 1;
     for (int gq = mt * 4; !hit && gq < min(ngroups, mt * 4 + 4); ++gq) {
       const float ml = minlse2[gq];
       if (ml == INFINITY) continue;
+      if (!in_bounds(P.status, m0 / 32 + gq, ((int64_t)P.M + 31) / 32) ||
+          !in_bounds(P.status, v0 / 256 + vt, P.bmax_ld)) {
+        hit = 1;
+        break;
+      }
       const float bm = __ldg(P.bmax + (size_t)(m0 / 32 + gq) * P.bmax_ld + (v0 / 256 + vt));
       hit = bm - ml >= P.thr2 - kMargin;  // -inf block maxima (no supervised row) never hold work
     }
@@ -122,7 +130,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const SkipPlan P) {
     if (!keep[k]) continue;
     int mt, vt;
     chunk_decode(kPerThread * tid + k, n_mt, n_vt, chunk, mt, vt);
-    list[pos++] = vt * n_mt + mt;
+    if (in_bounds(P.status, pos, (int64_t)P.shape.n_mt * P.shape.n_vt)) list[pos] = vt * n_mt + mt;
+    ++pos;
   }
   if (tid == kPlanThreads - 1) *count = warp_sums[31];
 }
