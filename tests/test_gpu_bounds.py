@@ -47,3 +47,11 @@ def test_bounds_checked_build_matches_release(tmp_path):
         assert int(release["status"][0]) == 0
         for k in ("logp", "lse", "out", "g", "dh", "dW"):
             assert np.array_equal(checked[k], release[k], equal_nan=True), (name, mode, k)
+
+
+def test_suite_runs_on_the_library_it_was_asked_for(request):
+    # under --bounds-checked every test of the session goes through liborpo_head_debug.so
+    lib = orpo.load()
+    want = "liborpo_head_debug.so" if request.config.getoption("--bounds-checked") else "liborpo_head.so"
+    assert os.path.basename(lib._name) == want
+    assert os.path.basename(orpo.lib_path()) == want
