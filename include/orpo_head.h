@@ -122,8 +122,9 @@ int orpo_head_fwd(const void* h_bf16, const void* W_bf16, const int32_t* targets
  *   g[t] = dloss/dlogp[t] = mask[t] * G_{s(t)} / n_{s(t)}, with
  *          G_w = (-1 - lambda * sigmoid(-x) / (1 - e^{l_w})) / P,
  *          G_r = ( lambda * sigmoid(-x) / (1 - e^{l_r})) / P;  g = 0 on pad rows.
- * Sums are taken in fp64 in a fixed order (bitwise reproducible); the per-pair
- * transcendentals are evaluated in fp32 on fp64-formed arguments.
+ * Sums, means and per-pair differences are taken in two-float arithmetic (pairs
+ * of fp32 values, about 48 significant bits) in a fixed order (bitwise
+ * reproducible); the per-pair transcendentals and gradients are fp32.
  * Device errors: ORPO_STATUS_SEQID, ORPO_STATUS_EMPTY_SEQ, ORPO_STATUS_NONFINITE
  * (e.g. l = 0 makes log1mexp -inf; it is reported, not clamped).
  * Limits: 1 <= n_pairs <= ORPO_MAX_PAIRS, 0 <= M <= 2^31 - 2^16, lambda >= 0.
