@@ -71,11 +71,18 @@ struct BwdBlocks {
   int64_t Mc, Vc;  // rows / columns of the scratch block (multiples of 128 / 256)
 };
 
-BwdBlocks bwd_blocks(int64_t M, int64_t V) {
+// quantised head: the bf16 copy of W is made one vocabulary block at a time within this budget
+constexpr int64_t kWBlockBudget = 256ll << 20;
+
+// qd > 0: the quantised head of hidden size qd, whose vocabulary block must also fit the bf16
+// W-block budget (with few rows the dZ budget alone would allow the whole vocabulary, and the
+// dequantised copy would be all of W)
+BwdBlocks bwd_blocks(int64_t M, int64_t V, int64_t qd = 0) {
   const int64_t Mpad = std::max<int64_t>(kBM, cdiv(M, kBM) * kBM);
   const int64_t Mc = std::min(Mpad, kMcMax);
   const int64_t Vpad = cdiv(V, kBN) * kBN;
   int64_t vc = (kScratchBudget / (2 * Mc)) / kBN * kBN;
+  if (qd > 0) vc = std::min<int64_t>(vc, (kWBlockBudget / (2 * qd)) / kBN * kBN);
   vc = std::max<int64_t>(kBN, vc);
   return BwdBlocks{Mc, std::min(Vpad, vc)};
 }
@@ -86,9 +93,8 @@ size_t partial_bytes(int64_t M, int nsplit_max) {
   return (size_t)2 * nsplit_max * Mpad * sizeof(float);
 }
 
-// quantised head: most splits over all dequantised blocks, and the bf16 block of W
+// quantised head: most splits over all dequantised blocks
 constexpr int kNsplitMaxQ = 256;
-constexpr int64_t kWBlockBudget = 256ll << 20;
 
 void* align_ws(void* ws) {
   uintptr_t p = reinterpret_cast<uintptr_t>(ws);
@@ -108,7 +114,7 @@ size_t scratch_bytes(int64_t M, int64_t V) {
 // Rows of W dequantised at a time: a multiple of the backward's vocabulary block (so the backward
 // reuses the same buffer block by block) within kWBlockBudget bytes of bf16, at least one block.
 int64_t wblock_rows(int64_t M, int64_t V, int64_t d) {
-  const BwdBlocks b = bwd_blocks(M, V);
+  const BwdBlocks b = bwd_blocks(M, V, d);
   const int64_t fit = kWBlockBudget / (2 * d);
   const int64_t k = std::max<int64_t>(1, fit / b.Vc);
   return std::min(cdiv(V, kBN) * kBN, k * b.Vc);
@@ -362,7 +368,7 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
     return cudaMemsetAsync(dW, 0, (size_t)V * d * sizeof(float), st) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
   }
 
-  const BwdBlocks B = bwd_blocks(M, V);
+  const BwdBlocks B = bwd_blocks(M, V, q ? d : 0);
   void* S = align_ws(workspace);
   int* counters = reinterpret_cast<int*>(static_cast<uint8_t*>(S) + scratch_bytes(M, V));
   // backward skips: plan rounds over the blocks, slots in the area after the counters

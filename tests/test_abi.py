@@ -156,3 +156,14 @@ def test_quantised_skip_host_checks(lib):
     assert fwd(bm=ctypes.c_void_p(0x10002)) == ERR_ALIGN
     assert bwd(eps=-1.0) == ERR_ARG
     assert bwd(bits=5) == ERR_ARG
+
+
+def test_quantised_workspace_stays_bounded(lib):
+    # the dequantised W block keeps to its 256 MiB budget at every M, also when few rows would let the
+    # dZ block span the whole vocabulary; the whole quantised workspace stays far below a bf16 copy of W
+    for V, d in ((262144, 2560), (128256, 4096), (32000, 2048)):
+        for M in (1, 128, 512, 2048, 8192, 65536):
+            q = orpo.orpo_head_q_workspace_bytes(M, V, d)
+            b = orpo.orpo_head_workspace_bytes(M, V, d)
+            assert 0 < q - b <= (256 << 20) + (192 << 20), (V, d, M, q, b)   # W block + larger split table
+            assert q <= (520 << 20), (V, d, M, q)
