@@ -2,7 +2,8 @@
 hold more than 2^31 elements, with a ragged V = 300 and the softcap on.  Forward, loss and backward
 run over every row; the oracle checks seeded sample rows (the last rows among them), the whole loss
 and gradient g, and all of dh and dW for a cotangent supported on sampled rows.  Inputs are drawn on
-the device from a seeded generator and the sampled rows copied back for the oracle."""
+the device from a seeded generator and the sampled rows copied back for the oracle.  A vocabulary
+of 2^20 + 37 columns checks the other extreme: the most forward splits and a ragged last tile."""
 
 import numpy as np
 import pytest
@@ -103,3 +104,44 @@ def test_backward_past_32_bit_offsets(big):
     nz = torch.nonzero(dh.abs().amax(dim=1) != 0).flatten().cpu().numpy()
     assert set(nz.tolist()) <= set(rows.tolist())
     assert bool(torch.isfinite(dh).all())
+
+
+def test_vocabulary_past_2_20_with_a_ragged_tail():
+    # V = 2^20 + 37 at small M: the forward runs its most splits with many tiles each, and the
+    # backward's vocabulary blocks end in a 37-column tile; every row is checked, and dh and dW
+    # exactly for a cotangent on a few rows
+    Mv, Dv, Vv, cap = 256, 64, (1 << 20) + 37, 30.0
+    g = torch.Generator(device=dev()).manual_seed(7)
+    h = torch.randn((Mv, Dv), generator=g, device=dev()).to(torch.bfloat16)
+    W = (torch.randn((Vv, Dv), generator=g, device=dev()) * (2.0 / Dv ** 0.5)).to(torch.bfloat16)
+    tg = torch.randint(0, Vv, (Mv,), generator=g, device=dev(), dtype=torch.int32)
+    tg[:4] = torch.tensor([Vv - 1, Vv - 37, Vv - 38, 0], dtype=torch.int32)  # targets in and next to the tail
+    mk = torch.ones(Mv, dtype=torch.uint8, device=dev())
+    ws = torch.empty(orpo.orpo_head_workspace_bytes(Mv, Vv, Dv), dtype=torch.uint8, device=dev())
+    logp = torch.empty(Mv, device=dev())
+    lse = torch.empty(Mv, device=dev())
+    st = torch.zeros(1, dtype=torch.int32, device=dev())
+    orpo.orpo_head_fwd(h, W, tg, mk, cap, logp, lse, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    h64, W64 = oracle.bf16_bits_to_f64(bits(h)), oracle.bf16_bits_to_f64(bits(W))
+    tgn, mkn = tg.cpu().numpy(), mk.cpu().numpy()
+    rl, rs = oracle.head_forward(h64, W64, tgn, mkn, cap)
+    assert np.max(np.abs(lse.cpu().numpy() - rs)) < LOGP_ATOL
+    assert np.max(np.abs(logp.cpu().numpy() - rl)) < LOGP_ATOL
+
+    rows = np.array([0, 1, 2, 3, 100, 255])
+    gv = np.zeros(Mv, dtype=np.float32)
+    gv[rows] = (np.random.default_rng(3).standard_normal(len(rows)) * 1e-3).astype(np.float32)
+    dh = torch.full((Mv, Dv), float("nan"), device=dev())
+    dW = torch.full((Vv, Dv), float("nan"), device=dev())
+    orpo.orpo_head_bwd(h, W, tg, mk, lse, torch.from_numpy(gv).to(dev()), cap, dh, dW, False, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    lse_n = lse.cpu().numpy()
+    rdh, rdW = oracle.head_backward(h64[rows], W64, tgn[rows], mkn[rows], lse_n[rows], gv[rows], cap)
+    assert relfro(dh.cpu().numpy()[rows], rdh) < GRAD_RELFRO
+    assert relfro(dW.cpu().numpy(), rdW) < GRAD_RELFRO
+    other = np.ones(Mv, dtype=bool)
+    other[rows] = False
+    assert np.all(dh.cpu().numpy()[other] == 0)
