@@ -367,22 +367,30 @@ def ours(args, w, rank, world, local):
         copied = [torch.cuda.Event(), torch.cuda.Event()]
         freed = [torch.cuda.Event(), torch.cuda.Event()]
 
-        def issue_copy(k):
+        copy_times = []   # (start, end) events of each timed step's copy, for the measured H2D rate
+
+        def issue_copy(k, timing=None):
             b = k % 2
             with torch.cuda.stream(copy_stream):
                 if k >= 2:
                     copy_stream.wait_event(freed[b])   # step k - 2 is done with this set
+                if timing is not None:
+                    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    c0.record(copy_stream)
                 for name in host:
                     sets[b][name].copy_(host[name], non_blocking=True)
+                if timing is not None:
+                    c1.record(copy_stream)
+                    timing.append((c0, c1))
                 copied[b].record(copy_stream)
 
-        def run_e2e(steps, start):
+        def run_e2e(steps, start, timing=None):
             start.record(stream)
             copy_stream.wait_event(start)
-            issue_copy(0)
+            issue_copy(0, timing)
             for k in range(steps):
                 if k + 1 < steps:
-                    issue_copy(k + 1)
+                    issue_copy(k + 1, timing)
                 stream.wait_event(copied[k % 2])
                 step(sets[k % 2])
                 freed[k % 2].record(stream)
@@ -395,7 +403,7 @@ def ours(args, w, rank, world, local):
         barrier()
         torch.cuda.synchronize()
         e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        run_e2e(args.steps, e2)
+        run_e2e(args.steps, e2, copy_times)
         e3.record(stream)
         torch.cuda.synchronize()
         ms2 = e2.elapsed_time(e3)
@@ -403,9 +411,11 @@ def ours(args, w, rank, world, local):
             x = torch.tensor([ms2], device=dev)
             dist.all_reduce(x, op=dist.ReduceOp.MAX)
             ms2 = float(x.item())
+        copy_ms = sorted(c0.elapsed_time(c1) for c0, c1 in copy_times)
         e2e = {"value": world * M * args.steps / (ms2 / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h,
-               "pipelining": "inputs of step k+1 copied on a second stream while step k computes"}
+               "pipelining": "inputs of step k+1 copied on a second stream while step k computes",
+               "h2d_gb_per_s_median": h2d / (copy_ms[len(copy_ms) // 2] / 1e3) / 1e9 if copy_ms else None}
     st = int(status.item())
     if st != 0:
         raise RuntimeError(f"device status after timing: {orpo.orpo_status_string(st)}")
