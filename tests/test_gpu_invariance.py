@@ -50,3 +50,48 @@ def test_unsupervised_rows_inserted_anywhere_change_nothing(name, kw):
     assert np.allclose(b["g"][real], a["g"], rtol=1e-5, atol=1e-12)
     assert relfro(b["dh"][real], a["dh"]) < 1e-4
     assert relfro(b["dW"], a["dW"]) < 1e-4
+
+
+def test_vocabulary_permutation_moves_only_dW_rows():
+    # relabel the vocabulary: W'[j] = W[perm[j]], y' = perm^-1[y].  Every logit is the same number in
+    # another column, so logp, lse, the loss and dh stay put (to fp32 reordering of the sums) and
+    # dW'[j] = dW[perm[j]]; a wrong column offset in any split or vocabulary block would show here
+    w = workloads.make("e4b", M=2048, d=128, V=65536 + 320)
+    perm = np.random.default_rng(8).permutation(w.V)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(w.V)
+    wp = dataclasses.replace(w, W=np.ascontiguousarray(w.W[perm]), targets=inv[w.targets].astype(np.int32))
+    a, b = run_chain(w), run_chain(wp)
+    assert np.max(np.abs(b["logp"] - a["logp"])) < 1e-5
+    assert np.max(np.abs(b["lse"] - a["lse"])) < 1e-5
+    assert np.allclose(b["out"], a["out"], rtol=1e-5, atol=1e-7)
+    assert relfro(b["dh"], a["dh"]) < 1e-4
+    assert relfro(b["dW"], a["dW"][perm]) < 1e-4
+
+
+def test_pair_order_moves_only_rows():
+    # reorder the pairs (rows of each sequence move with it, ids relabelled in the new order): the loss
+    # is a mean over pairs and dW a sum over rows, so both stay put; per-row outputs move with the rows
+    w = workloads.make("small")
+    P = w.n_pairs
+    sigma = np.random.default_rng(4).permutation(P)
+    order, new_sid = [], []
+    for q, p in enumerate(sigma):
+        for k in (0, 1):
+            rows = np.where(w.seq_id == 2 * p + k)[0]
+            order.append(rows)
+            new_sid.append(np.full(len(rows), 2 * q + k, np.int32))
+    pad = np.where(w.seq_id < 0)[0]
+    order = np.concatenate(order + [pad])
+    new_sid = np.concatenate(new_sid + [np.full(len(pad), -1, np.int32)])
+    assert len(order) == w.M
+    wp = dataclasses.replace(w, h=np.ascontiguousarray(w.h[order]), targets=w.targets[order],
+                             mask=w.mask[order], seq_id=new_sid)
+    a, b = run_chain(w), run_chain(wp)
+    assert np.max(np.abs(b["logp"] - a["logp"][order])) < 1e-5
+    assert np.allclose(b["out"], a["out"], rtol=1e-5, atol=1e-7)
+    ell_new = a["ell"].reshape(P, 2)[sigma].reshape(-1)
+    assert np.allclose(b["ell"], ell_new, rtol=1e-6, atol=1e-7)
+    assert np.allclose(b["g"], a["g"][order], rtol=1e-5, atol=1e-12)
+    assert relfro(b["dh"], a["dh"][order]) < 1e-4
+    assert relfro(b["dW"], a["dW"]) < 1e-4
