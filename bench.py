@@ -108,23 +108,25 @@ def kernel_sources_sha(kernel):
     return h.hexdigest()[:16]
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_e4b.json")
+
+
 def profiled_traffic(w, kernel):
-    """DRAM bytes per launch of `kernel` from the committed full-size ncu capture, or None when the
-    workload differs from the captured one or the kernel sources changed since the capture."""
+    """DRAM bytes per launch of `kernel` at the e4b shape, from the committed ncu capture record
+    (profiles/traffic_e4b.json: a small-case capture scaled to one e4b launch), or None when the
+    workload differs from e4b or the kernel sources changed since the capture."""
     if (w.name, w.M, w.d, w.V) != ("e4b", 8192, 2560, 262144):
         return None
     try:
-        text = open(os.path.join(ROOT, "profiles", "ncu_traffic_e4b.md")).read()
-    except OSError:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    for line in text.splitlines():
-        if line.startswith("traffic_bytes_per_launch"):
-            fields = dict(kv.split("=") for kv in line.split()[1:])
-            if kernel not in KERNEL_SOURCES or fields.get("sources_" + kernel) != kernel_sources_sha(kernel):
-                return None
-            v = fields.get(kernel)
-            return int(v) if v is not None else None
-    return None
+    k = rec.get("kernels", {}).get(kernel)
+    if not k or kernel not in KERNEL_SOURCES or k.get("sources_sha") != kernel_sources_sha(kernel):
+        return None
+    v = k.get("bytes_per_e4b_launch")
+    return int(v) if v is not None else None
 
 
 # ---------------------------------------------------------------- clocks during the timed region
@@ -215,6 +217,34 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def blas_threads():
+    """Threads of the BLAS that numpy (and so the oracle) calls, or None when it cannot be read."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    try:  # numpy's bundled OpenBLAS, asked directly (threadpoolctl is not always installed)
+        import ctypes
+        with open("/proc/self/maps") as f:
+            libs = sorted({ln.split()[-1] for ln in f if "openblas" in ln.split()[-1].lower()})
+        for path in libs:
+            lib = ctypes.CDLL(path)
+            for name in ("openblas_get_num_threads", "openblas_get_num_threads64_",
+                         "scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads"):
+                fn = getattr(lib, name, None)
+                if fn is not None:
+                    return int(fn())
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return None
+
+
 def reference_arm(args, w, rank, world):
     """Times the float64 oracle, as it stands, on a bounded sample of the workload."""
     if rank != 0:
@@ -234,8 +264,8 @@ def reference_arm(args, w, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": cfg,
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "blas_threads": blas_threads(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -444,9 +474,12 @@ def ours(args, w, rank, world, local):
     per_launch_flops = kflops[dom] / kernels[dom]["launches"]
     achieved = per_launch_flops / (kernels[dom]["ms_per_launch"] / 1e3) / 1e12
     traffic = profiled_traffic(w, dom)
-    roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
-            "frac": achieved / sustained, "traffic": traffic,
-            "peak_source": f"{src} bf16 sustained (MEASURED_PEAKS.json bf16_tflops_sustained)"}
+    # the step lasts tens of milliseconds, so its kernels are judged against the burst peak; the
+    # seconds-long power-capped figure is reported beside it
+    roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
+            "frac": achieved / burst, "traffic": traffic,
+            "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
+            "peak_sustained": sustained, "frac_of_sustained": achieved / sustained}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -456,7 +489,7 @@ def ours(args, w, rank, world, local):
                            backward=(f"skips at eps {args.skip_eps:g} (coefficient filter + block skip); "
                                      "tflops counts the dense 6MVd" if skip else "exact"),
                            parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
-            "tflops": tflops, "frac_of_peak": tflops / sustained, "frac_of_burst_peak": tflops / burst,
+            "tflops": tflops, "frac_of_peak": tflops / burst, "frac_of_sustained_peak": tflops / sustained,
             "peak_extra_gb": peak_extra / 1e9, "e2e": e2e, "gpu_launches": sum(v["launches"] for v in
                                                                                kernels.values()),
             "kernels": kernels, "roofline": roof, "clocks": clk}
@@ -465,7 +498,7 @@ def ours(args, w, rank, world, local):
         del t, host
         secs = run_oracle_sample(w, idx, oracle_weights(w))
         line["cpu_baseline"] = {"value": len(idx) / secs, "unit": "tokens/s", "cores": cpu_cores(),
-                                "kind": "oracle",
+                                "blas_threads": blas_threads(), "kind": "oracle",
                                 "sample": f"{sample_text(w, idx)}, float64 forward + loss + backward, {secs:.1f} s"}
     print(json.dumps(line), flush=True)
 

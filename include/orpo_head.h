@@ -309,8 +309,12 @@ int orpo_debug_gemm(const void* A_bf16, const void* B_bf16, float* C, int64_t M,
  *     and launches nothing.  Large M may use fewer vocabulary splits than
  *     orpo_head_fwd (results agree to rounding).
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current).  Under lazy module
+ *     loading (the CUDA default since 12.2) that lookup is also what loads the
+ *     library's host-side module on the device and reserves the 4 MiB, so it can
+ *     fail with ORPO_ERR_CUDA if the device is already out of memory.  A caller
+ *     with a fixed memory budget makes that first call (any M >= 1) at start-up,
+ *     before it fixes the budget and before any stream capture.
  *   - Every call on a device shares the one array, which keeps the last call's
  *     contents; nothing in it needs to start at zero (every entry read was
  *     written by the same call).  Calls whose GPU work overlaps in time (other
