@@ -160,19 +160,21 @@ int choose_nsplit(int64_t n_mt, int64_t n_vt, int sms) {
   return best;
 }
 
-// Forward launch shape.  Pair mode (2-CTA clusters sharing each W tile) when at least two row
-// tiles exist and padding an odd count to even wastes little; then the units along M are row-tile
-// pairs and the slots are co-resident clusters.
-struct FwdShape {
-  int pair;
-  int64_t units_m;  // row tiles, or row-tile pairs in pair mode
-  int slots;        // CTAs, or clusters in pair mode
+// Engine placement on the current device: 2-CTA clusters (slots = clusters) or single CTAs (slots =
+// SMs).  By default only the dh / dW GEMM (`gemm`) takes clusters: in the power-capped e4b step the
+// forward and the recompute ran faster on single CTAs and the GEMM on clusters.  ORPO_CTA_GROUP
+// forces one form; `allow_pair` false forces single CTAs (the backward skips' per-tile bitmaps and
+// lists), as does a device where no cluster fits.
+struct Placement {
+  int cg;
+  int slots;
 };
 
-FwdShape forward_shape(int64_t n_mt, int sms) {
-  const int clusters = (n_mt >= 2 && (n_mt % 2 == 0 || n_mt >= 16)) ? forward_pair_clusters() : 0;
-  if (clusters > 0) return FwdShape{1, (n_mt + 1) / 2, clusters};
-  return FwdShape{0, n_mt, sms};
+Placement placement(int sms, bool gemm, bool allow_pair = true) {
+  const int force = engine_cta_group_override();
+  const bool want = allow_pair && (force == 2 || (force == 0 && gemm));
+  const int clusters = want ? engine_pair_clusters() : 0;
+  return clusters > 0 ? Placement{2, clusters} : Placement{1, sms};
 }
 
 }  // namespace
@@ -277,10 +279,11 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   const int64_t nblocks = cdiv(V, vb);
   const int per_block = std::max<int>(1, nsplit_max / (int)nblocks);
   void* Wb = q ? wblock_ptr(workspace, M, V) : nullptr;
-  const FwdShape fs = forward_shape(n_mt, sms);
-  L.pair = fs.pair;
-  L.chunk = l2_chunk((int)fs.units_m, (int64_t)(fs.pair ? 2 : 1) * kBM * d * 2);
-  const uint32_t w_box = fs.pair ? kBN / 2 : kBN;
+  const Placement pl = placement(sms, false);
+  const int64_t n_mu = cdiv(n_mt, pl.cg);  // M units: row tiles, or pairs of them
+  L.cg = pl.cg;
+  L.chunk = l2_chunk((int)n_mu, (int64_t)pl.cg * kBM * d * 2);
+  const uint32_t w_box = kBN / pl.cg;
   int split0 = 0;
   for (int64_t v0 = 0; v0 < V; v0 += vb) {
     const int64_t vc = std::min(vb, V - v0);
@@ -293,10 +296,10 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
       return ORPO_ERR_CUDA;
     }
     L.n_vt = (int)n_vt;
-    L.nsplit = std::min<int>(choose_nsplit(fs.units_m, n_vt, fs.slots), per_block);
+    L.nsplit = std::min<int>(choose_nsplit(n_mu, n_vt, pl.slots), per_block);
     L.col0 = (int)v0;
     L.split0 = split0;
-    L.grid = (int)std::min<int64_t>(fs.units_m * L.nsplit, fs.slots) * (fs.pair ? 2 : 1);
+    L.grid = (int)std::min<int64_t>(n_mu * L.nsplit, pl.slots) * pl.cg;
     if (launch_forward_logits(L, st) != cudaSuccess) return ORPO_ERR_CUDA;
     split0 += L.nsplit;
   }
@@ -392,6 +395,10 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   void* Wb = q ? wblock_ptr(workspace, M, V) : nullptr;
   int64_t launch = 0;
   const int64_t sp = scratch_pitch(B);
+  // the skips' bitmaps and tile lists are per 128-row tile
+  const Placement pr = placement(sms, false, !skip);  // recompute
+  const Placement pl = placement(sms, true, !skip);   // dh / dW GEMM
+  const uint32_t b_rows = kBN / pl.cg;                // rows or columns of the GEMMs' B per CTA
   const bool d64 = d % 64 == 0;  // MN-major h / W fetched with one 3-D box per stage
   RecLaunch R;
   GemmLaunch G;
@@ -400,7 +407,7 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
             // gemm maps: 0 S K-major rows, 1 W MN-major, 2 S MN-major, 3 h MN-major, 4 dh, 5 dW
             encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, S, B.Vc, B.Mc, sp * 2, 64, kBM) &&
             encode_map_mn3d(&G.maps[2], S, B.Vc, B.Mc, sp * 2, kBM / 64) &&
-            (d64 ? encode_map_mn3d(&G.maps[3], h, d, M, d * 2, kBN / 64)
+            (d64 ? encode_map_mn3d(&G.maps[3], h, d, M, d * 2, b_rows / 64)
                  : encode_map_2d(&G.maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, 64)) &&
             encode_map_2d(&G.maps[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dh, d, M, d * 4, 32, 32) &&
             (!dW || encode_map_2d(&G.maps[5], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, d, V, d * 4, 32, 32));
@@ -408,12 +415,14 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   if (!dW) G.maps[5] = G.maps[4];
   // W maps over the whole bf16 head (encoded once), or per block over the dequantised copy
   auto encode_w = [&](const void* base, int64_t rows) {
-    return encode_map_2d(&R.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d, rows, d * 2, 64, kBN) &&
-           (d64 ? encode_map_mn3d(&G.maps[1], base, d, rows, d * 2, kBN / 64)
+    return encode_map_2d(&R.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d, rows, d * 2, 64, kBN / pr.cg) &&
+           (d64 ? encode_map_mn3d(&G.maps[1], base, d, rows, d * 2, b_rows / 64)
                 : encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d, rows, d * 2, 64, 64));
   };
   if (!q && !encode_w(W, V)) return ORPO_ERR_CUDA;
   G.status = status;
+  G.cg = pl.cg;
+  R.cg = pr.cg;
   R.targets = targets;
   R.mask = mask;
   R.lse = lse;
@@ -441,8 +450,9 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
       R.w_row0 = q ? 0 : (int)v0;
       R.n_mt = n_mt;
       R.n_vt = n_vt;
-      R.chunk = l2_chunk(n_mt, (int64_t)kBM * d * 2);
-      R.grid = (int)std::min<int64_t>((int64_t)n_mt * n_vt, sms);
+      const int64_t n_mu = cdiv(n_mt, pr.cg);
+      R.chunk = l2_chunk((int)n_mu, (int64_t)pr.cg * kBM * d * 2);
+      R.grid = (int)std::min<int64_t>(n_mu * n_vt, pr.slots) * pr.cg;
       uint32_t *rowbits = nullptr, *colbits = nullptr;
       if (skip) {
         const int64_t slot = block % round_slots;
@@ -476,8 +486,8 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
         G.cls[0] = cdh;
         G.cls[1] = cdw;
       }
-      const int64_t units = (int64_t)cdw.n_mt * cdw.n_nt + (int64_t)cdh.n_mt * cdh.n_nt;
-      G.grid = (int)std::min<int64_t>(units, sms);
+      const int64_t units = cdiv(cdw.n_mt, pl.cg) * cdw.n_nt + cdiv(cdh.n_mt, pl.cg) * cdh.n_nt;
+      G.grid = (int)std::min<int64_t>(units, pl.slots) * pl.cg;
       if (launch % kCounters == 0 && cudaMemsetAsync(counters, 0, kCounterBytes, st) != cudaSuccess)
         return ORPO_ERR_CUDA;
       G.counter = counters + (launch++ % kCounters);
@@ -620,15 +630,17 @@ int orpo_debug_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N
   if (int e = device_check(&sms)) return e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   GemmLaunch G;
+  const Placement pl = placement(sms, true);
+  const uint32_t b_rows = kBN / pl.cg;
   // MN-major operands whose contiguous extent is a multiple of 64 use the one-box 3-D fetch
   const int a_mode = a_mn_major ? (M % 64 == 0 ? 2 : 1) : 0;
   const int b_mode = b_mn_major ? (N % 64 == 0 ? 2 : 1) : 0;
   bool ok = a_mode == 2   ? encode_map_mn3d(&G.maps[0], A, M, K, M * 2, kBM / 64)
             : a_mode == 1 ? encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, M, K, M * 2, 64, 64)
                           : encode_map_2d(&G.maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, K * 2, 64, kBM);
-  ok = ok && (b_mode == 2   ? encode_map_mn3d(&G.maps[1], B, N, K, N * 2, kBN / 64)
+  ok = ok && (b_mode == 2   ? encode_map_mn3d(&G.maps[1], B, N, K, N * 2, b_rows / 64)
               : b_mode == 1 ? encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, N * 2, 64, 64)
-                            : encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, K * 2, 64, kBN));
+                            : encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, K * 2, 64, b_rows));
   ok = ok && encode_map_2d(&G.maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, N * 4, 32, 32);
   if (!ok) return ORPO_ERR_CUDA;
   G.maps[3] = G.maps[4] = G.maps[5] = G.maps[0];
@@ -641,7 +653,8 @@ int orpo_debug_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N
   G.cls[1] = GemmClassH{};
   G.counter = nullptr;
   G.status = status;
-  G.grid = (int)std::min<int64_t>((int64_t)c.n_mt * c.n_nt, sms);
+  G.cg = pl.cg;
+  G.grid = (int)std::min<int64_t>(cdiv(c.n_mt, pl.cg) * c.n_nt, pl.slots) * pl.cg;
   return launch_gemm(G, st, K_DEBUG) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
 }
 
@@ -734,13 +747,17 @@ extern "C" int orpo_head_fwd_static(const void* h, const void* W, const int32_t*
   FwdLaunch L;
   const int64_t n_mt = cdiv(M, kBM), n_vt = cdiv(V, kBN);
   const int64_t Mpad = n_mt * kBM;
+  const Placement pl = placement(sms, false);
+  const int64_t n_mu = cdiv(n_mt, pl.cg);
   if (!encode_map_2d(&L.mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, kBM) ||
-      !encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, kBN))
+      !encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, kBN / pl.cg))
     return ORPO_ERR_CUDA;
   const int cap = (int)std::max<int64_t>(1, kStaticFloats / (2 * Mpad));
+  L.cg = pl.cg;
+  L.chunk = l2_chunk((int)n_mu, (int64_t)pl.cg * kBM * d * 2);
   L.n_mt = (int)n_mt;
   L.n_vt = (int)n_vt;
-  L.nsplit = std::min(choose_nsplit(n_mt, n_vt, sms), cap);
+  L.nsplit = std::min(choose_nsplit(n_mu, n_vt, pl.slots), cap);
   L.kblocks = (int)cdiv(d, 64);
   L.targets = targets;
   L.mask = mask;
@@ -754,6 +771,6 @@ extern "C" int orpo_head_fwd_static(const void* h, const void* W, const int32_t*
   L.V = (int)V;
   L.softcap = softcap > 0.f ? softcap : 0.f;
   L.status = status;
-  L.grid = (int)std::min<int64_t>(n_mt * L.nsplit, sms);
+  L.grid = (int)std::min<int64_t>(n_mu * L.nsplit, pl.slots) * pl.cg;
   return launch_forward(L, st) == cudaSuccess ? ORPO_OK : ORPO_ERR_CUDA;
 }

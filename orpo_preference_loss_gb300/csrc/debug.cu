@@ -17,7 +17,7 @@ __global__ void wait_timeout_kernel(int32_t* status, uint64_t limit_ns) {
   ctl.abort_flag = 0;
   mbar_init(&ctl.drain, 1);
   fence_mbar_init();
-  wait_phase(&ctl, &ctl.drain, 0, status, limit_ns);  // nobody arrives on this barrier
+  wait_phase<1>(&ctl, &ctl.drain, 0, status, limit_ns);  // nobody arrives on this barrier
 }
 
 }  // namespace

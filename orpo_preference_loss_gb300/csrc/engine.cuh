@@ -1,22 +1,33 @@
 // engine.cuh — persistent, warp-specialised tcgen05 GEMM pipeline shared by every
 // contraction of the head (forward logits, backward logit recompute, dh and dW).
 //
-// One CTA per SM.  Warp 0 issues TMA loads into a STAGES-deep shared-memory ring,
+// One CTA per SM.  Warp 0 issues TMA loads into a shared-memory ring of stages,
 // warp 1 issues tcgen05.mma (one thread) into a double-buffered TMEM accumulator
 // (2 x 256 fp32 columns = all 512 columns), warps 2..5 run the epilogue that the
-// kernel supplies.  Each accumulator tile is BM x BN = 128 x 256, built from BK = 64
-// wide k-blocks (128-byte swizzle rows) of bf16 operands.
+// kernel supplies.  Each CTA's accumulator tile is BM x BN = 128 x 256, built from
+// BK = 64 wide k-blocks (128-byte swizzle rows) of bf16 operands.
 //
-// Operand staging in shared memory (per stage: A 16 KiB, B 32 KiB):
+// Two forms, chosen by the template argument CG (the tcgen05 CTA group):
+//   CG = 1  one CTA per tile.  A stage holds A (128 x 64) and B (256 x 64): 48 KiB, 4 stages.
+//   CG = 2  a 2-CTA cluster computes a 256 x 256 tile with tcgen05.mma.cta_group::2, issued by
+//           the even CTA.  Each CTA fetches its own 128 rows of A and its own half (128 rows)
+//           of B into its own shared memory with plain (non-multicast) TMA loads, whose bytes
+//           are counted on the even CTA's `full` barrier; each CTA's tensor memory receives its
+//           128 rows of the accumulator.  A stage is 32 KiB, so 6 stages fit where 4 did, and
+//           every B tile crosses from L2 once per 256 rows instead of once per 128.  The even
+//           CTA's commits free the stages and publish the accumulators in both CTAs (two
+//           unicast commits, one per CTA); the odd CTA's epilogue warps release accumulators
+//           and unit slots by remote arrivals on the even CTA's barriers.
+//
+// Operand staging in shared memory (per stage: A 16 KiB, B 32 KiB / CG):
 //   K-major operand  [rows, K] with K contiguous: one TMA box {64 (K), rows};
 //                    rows at 128 B pitch, 8-row swizzle atoms 1024 B apart (SBO).
 //   MN-major operand [K, rows] with rows contiguous: rows/64 TMA boxes {64, 64},
 //                    each 64 k-rows x 128 B = 8 KiB (or one 3-D box over all of them);
 //                    LBO = 8 KiB between 64-wide column blocks, SBO = 1 KiB between
 //                    8-k-row groups.
-// Options a kernel picks: a paired mode (2-CTA clusters that multicast halves of the
-// B tile to each other, run_cta<true>), sparse K (a bitmap of k-block groups per tile,
-// KWalk), a static or a dynamic unit feed, and an L2-aware unit order (chunk_decode).
+// Options a kernel picks: sparse K (a bitmap of k-block groups per tile, KWalk; CG = 1 only), a
+// static or a dynamic unit feed, and an L2-aware unit order (chunk_decode).
 // Every wait is bounded: a wait that exceeds kWaitLimitNs sets ORPO_STATUS_TIMEOUT,
 // flags the CTA as aborted and every role drains its own in-flight work and returns.
 #pragma once
@@ -30,29 +41,40 @@ namespace orpo {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int MAX_STAGES = 6;
 constexpr int UMMA_K = 16;
 constexpr int EPI_WARPS = 4;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 512;
 
-constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KiB
-constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KiB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t A_BYTES = BM * BK * 2;            // 16 KiB
 constexpr uint32_t BOX_BYTES = 4096;                 // one 32-row x 128-byte epilogue staging box
 constexpr uint32_t STAGING_PER_WARP = 2 * BOX_BYTES;  // double-buffered
-constexpr uint32_t SMEM_STAGING_OFF = STAGES * STAGE_BYTES;
-constexpr uint32_t SMEM_CTL_OFF = SMEM_STAGING_OFF + EPI_WARPS * STAGING_PER_WARP;
 constexpr uint32_t SMEM_CTL_BYTES = 256;
-constexpr uint32_t SMEM_TOTAL = SMEM_CTL_OFF + SMEM_CTL_BYTES + 1024;  // + slack to align the base to 1 KiB
+
+// Shared-memory geometry of one CTA for CTA group CG.
+template <int CG>
+struct Geo {
+  static_assert(CG == 1 || CG == 2, "CTA group 1 or 2");
+  static constexpr int STAGES = CG == 2 ? 6 : 4;
+  static constexpr int B_ROWS = BN / CG;                // rows of the B tile this CTA fetches
+  static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;  // 32 KiB / CG
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TX_BYTES = CG * STAGE_BYTES;  // bytes one stage brings into the whole group
+  static constexpr uint32_t STAGING_OFF = STAGES * STAGE_BYTES;
+  static constexpr uint32_t CTL_OFF = STAGING_OFF + EPI_WARPS * STAGING_PER_WARP;
+  static constexpr uint32_t SMEM = CTL_OFF + SMEM_CTL_BYTES + 1024;  // + slack to align the base to 1 KiB
+  static_assert(STAGES <= MAX_STAGES, "control block holds MAX_STAGES stages");
+  static_assert(SMEM <= 232448, "dynamic shared memory per CTA");
+};
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far above any legitimate wait
 
 constexpr int RING = 4;                     // unit indices in flight between the roles (dynamic feed)
 
 struct SmemCtl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
@@ -62,57 +84,87 @@ struct SmemCtl {
   uint32_t tmem_base;
   volatile int abort_flag;
 };
+static_assert(sizeof(SmemCtl) <= SMEM_CTL_BYTES, "control block too large");
 
-// Source of work units.  Static: CTA b takes units b, b + G, b + 2G, ...
-// Dynamic (counter != nullptr): the producer thread claims the next unit with
-// an atomic add on a zeroed global counter and hands its index to the MMA and
-// epilogue warps through a RING-deep shared-memory ring; index -1 ends the
-// stream.  Every unit is still computed by exactly one CTA.
+// Source of work units.  Static: CTA (or 2-CTA cluster) b takes units b, b + G, b + 2G, ...
+// Dynamic (counter != nullptr): the producer thread (the even CTA's, in a pair) claims the next unit
+// with an atomic add on a zeroed global counter and hands its index to the MMA and epilogue warps
+// (and, in a pair, to the odd CTA's producer and epilogue warps) through a RING-deep shared-memory
+// ring; index -1 ends the stream.  Every unit is still computed by exactly one CTA or pair.
 struct Feed {
   int* counter;
   int nu;
-  int first = -1;  // static feed: first unit and stride (default: blockIdx.x, gridDim.x)
-  int stride = 0;
 };
 
+template <int CG>
 __device__ __forceinline__ int static_unit(const Feed& f, uint32_t i) {
-  const long long first = f.first >= 0 ? f.first : blockIdx.x;
-  const long long stride = f.stride > 0 ? f.stride : gridDim.x;
+  const long long first = CG == 2 ? (long long)cluster_id_x() : (long long)blockIdx.x;
+  const long long stride = CG == 2 ? (long long)num_clusters_x() : (long long)gridDim.x;
   const long long u = first + (long long)i * stride;
   return u < f.nu ? (int)u : -1;
 }
 
+template <int CG>
 __device__ __forceinline__ bool wait_phase(SmemCtl* ctl, uint64_t* bar, uint32_t parity, int32_t* status,
                                            uint64_t limit_ns = kWaitLimitNs);
 
-// Producer side: returns the next unit, -1 when done, -2 on abort.
-__device__ __forceinline__ int feed_produce(const Feed& f, SmemCtl* ctl, uint32_t i, int32_t* status) {
-  if (f.counter == nullptr) return static_unit(f, i);
+// rank of this CTA in its pair (0 for CG = 1)
+template <int CG>
+__device__ __forceinline__ uint32_t pair_rank() {
+  if constexpr (CG == 2)
+    return cluster_ctarank() & 1u;
+  else
+    return 0u;
+}
+
+// An arrival on barrier `bar` of the even CTA: local for the even CTA (and CG = 1), remote for the odd.
+template <int CG>
+__device__ __forceinline__ void arrive_leader(uint64_t* bar, uint32_t rank) {
+  if (CG == 2 && rank != 0)
+    mbar_arrive_cluster(mapa_u32(smem_u32(bar), 0));
+  else
+    mbar_arrive(bar);
+}
+
+// Producer side: returns the next unit, -1 when done, -2 on abort.  In a pair the odd CTA's producer
+// receives the even one's claims like the other consumers.
+template <int CG>
+__device__ __forceinline__ int feed_consume(const Feed& f, SmemCtl* ctl, uint32_t i, int32_t* status,
+                                            bool whole_warp, uint32_t rank);
+template <int CG>
+__device__ __forceinline__ int feed_produce(const Feed& f, SmemCtl* ctl, uint32_t i, int32_t* status, uint32_t rank) {
+  if (f.counter == nullptr) return static_unit<CG>(f, i);
+  if (CG == 2 && rank != 0) return feed_consume<CG>(f, ctl, i, status, false, rank);
   const uint32_t r = i % RING, ph = (i / RING) & 1u;
-  if (!wait_phase(ctl, &ctl->unit_empty[r], ph ^ 1u, status)) return -2;
+  if (!wait_phase<CG>(ctl, &ctl->unit_empty[r], ph ^ 1u, status)) return -2;
   int u = atomicAdd(f.counter, 1);
   if (u >= f.nu) u = -1;
   ctl->unit_ring[r] = u;
+  if constexpr (CG == 2) {  // the odd CTA's copy of the slot, then its notice
+    st_shared_cluster_u32(mapa_u32(smem_u32((const void*)&ctl->unit_ring[r]), 1), (uint32_t)u);
+    mbar_arrive_cluster(mapa_u32(smem_u32(&ctl->unit_full[r]), 1));
+  }
   mbar_arrive(&ctl->unit_full[r]);
   return u;
 }
 
-// Consumer side (the MMA thread, or a whole epilogue warp): same sequence as the producer's.
+// Consumer side (the MMA thread, a whole epilogue warp, or the odd CTA's producer): same sequence as
+// the producer's.
+template <int CG>
 __device__ __forceinline__ int feed_consume(const Feed& f, SmemCtl* ctl, uint32_t i, int32_t* status,
-                                            bool whole_warp) {
-  if (f.counter == nullptr) return static_unit(f, i);
+                                            bool whole_warp, uint32_t rank) {
+  if (f.counter == nullptr) return static_unit<CG>(f, i);
   const uint32_t r = i % RING, ph = (i / RING) & 1u;
-  if (!wait_phase(ctl, &ctl->unit_full[r], ph, status)) return -2;
+  if (!wait_phase<CG>(ctl, &ctl->unit_full[r], ph, status)) return -2;
   const int u = ctl->unit_ring[r];
   if (whole_warp) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->unit_empty[r]);
+    if ((threadIdx.x & 31) == 0) arrive_leader<CG>(&ctl->unit_empty[r], rank);
   } else {
-    mbar_arrive(&ctl->unit_empty[r]);
+    arrive_leader<CG>(&ctl->unit_empty[r], rank);
   }
   return u;
 }
-static_assert(sizeof(SmemCtl) <= SMEM_CTL_BYTES, "control block too large");
 
 // How one operand tile is fetched for one k-block.
 struct Operand {
@@ -129,6 +181,8 @@ struct Operand {
 // groups in ascending order, and kblocks (the count of set groups x 2^kg_shift, less what lies past
 // the operands' K extent in the last group) ends the walk.  A tile with kblocks == 0 issues no loads
 // and no MMAs and takes no accumulator; the kernel's epilogue handles it without waiting on one.
+// In a pair (CG = 2) a tile is this CTA's part of the pair's tile: its own 128 rows of A and its own
+// half of B; both CTAs' parts agree on kblocks and on the operand layouts.
 struct TileOps {
   Operand a, b;
   int kblocks;
@@ -191,13 +245,23 @@ __device__ __forceinline__ void chunk_decode(int u, int n_m, int n_n, int chunk,
   m = c * chunk + (local - n * rc);
 }
 
-// Bounded wait on an mbarrier phase.  Returns false on abort / timeout.
+// Bounded wait on an mbarrier phase.  Returns false on abort / timeout.  In a pair every barrier may
+// receive arrivals from the other CTA, so the wait acquires at cluster scope.
+template <int CG>
+__device__ __forceinline__ bool try_wait_cg(uint64_t* bar, uint32_t parity) {
+  if constexpr (CG == 2)
+    return mbar_try_wait_cluster(bar, parity);
+  else
+    return mbar_try_wait(bar, parity);
+}
+
+template <int CG>
 __device__ __forceinline__ bool wait_phase(SmemCtl* ctl, uint64_t* bar, uint32_t parity, int32_t* status,
                                            uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (try_wait_cg<CG>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_wait_cg<CG>(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (ctl->abort_flag) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
@@ -212,27 +276,35 @@ __device__ __forceinline__ bool wait_phase(SmemCtl* ctl, uint64_t* bar, uint32_t
 // Wait used while draining after an abort: short limit, ignores the abort flag.
 __device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_cluster(bar, parity)) {
     if (globaltimer_ns() - t0 > 200000000ull) return;
   }
 }
 
-__device__ __forceinline__ void load_operand(const Operand& op, uint64_t* bar, uint8_t* dst, int rows, int kb) {
-  if (op.mn_major == 0) {
-    tma_load_2d(op.map, bar, dst, op.k0 + kb * BK, op.mn0);
-  } else if (op.mn_major == 2) {
-    tma_load_3d(op.map, bar, dst, 0, op.k0 + kb * BK, op.mn0 / 64);
-  } else {
-    const int kk = op.k0 + kb * BK;
+// One operand tile of one k-block into `dst`; its bytes are counted on the barrier at shared::cluster
+// address `bar` (this CTA's own barrier for CG = 1, the even CTA's for CG = 2).
+template <int CG>
+__device__ __forceinline__ void load_operand(const Operand& op, uint32_t bar, uint8_t* dst, int rows, int kb) {
+  const int kk = op.k0 + kb * BK;
+  if constexpr (CG == 2) {
+    if (op.mn_major == 0) {
+      tma_load_2d_cg2(op.map, bar, dst, kk, op.mn0);
+    } else if (op.mn_major == 2) {
+      tma_load_3d_cg2(op.map, bar, dst, 0, kk, op.mn0 / 64);
+    } else {
 #pragma unroll 1
-    for (int c = 0; c < rows / 64; ++c) tma_load_2d(op.map, bar, dst + c * (BK * 128), op.mn0 + 64 * c, kk);
+      for (int c = 0; c < rows / 64; ++c) tma_load_2d_cg2(op.map, bar, dst + c * (BK * 128), op.mn0 + 64 * c, kk);
+    }
+  } else {
+    if (op.mn_major == 0) {
+      tma_load_2d(op.map, bar, dst, kk, op.mn0);
+    } else if (op.mn_major == 2) {
+      tma_load_3d(op.map, bar, dst, 0, kk, op.mn0 / 64);
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < rows / 64; ++c) tma_load_2d(op.map, bar, dst + c * (BK * 128), op.mn0 + 64 * c, kk);
+    }
   }
-}
-
-// Paired mode: this CTA fetches its half of the B tile (rows [rank * BN/2, (rank + 1) * BN/2) of a
-// K-major tile, through a map whose box is {64, BN/2}) and multicasts it to both CTAs of the cluster.
-__device__ __forceinline__ void load_b_half(const Operand& op, uint64_t* bar, uint8_t* b_dst, int kb, uint32_t rank) {
-  tma_load_2d_mc(op.map, bar, b_dst + rank * (B_BYTES / 2), op.k0 + kb * BK, op.mn0 + (int)rank * (BN / 2), 0x3);
 }
 
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, int kk) {
@@ -241,14 +313,15 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, in
                   : smem_desc_sw128(base + kk * (UMMA_K * 2), 16, 1024);
 }
 
-// ---------------------------------------------------------------- producer (one thread)
-template <bool kPair, class Sched>
-__device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* smem, SmemCtl* ctl, int32_t* status) {
-  const uint32_t rank = kPair ? cluster_ctarank() : 0;
+// ---------------------------------------------------------------- producer (one thread per CTA)
+template <int CG, class Sched>
+__device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* smem, SmemCtl* ctl, int32_t* status,
+                              uint32_t rank) {
+  using G = Geo<CG>;
   uint32_t it = 0;
   bool ok = true;
   for (uint32_t i = 0; ok; ++i) {
-    const int u = feed_produce(feed, ctl, i, status);
+    const int u = feed_produce<CG>(feed, ctl, i, status, rank);
     if (u < 0) {
       ok = (u == -1);
       break;
@@ -259,38 +332,49 @@ __device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* sme
       KWalk walk(t);
       for (int i = 0; i < t.kblocks; ++i, ++it) {
         const int kb = walk.kblock(i);
-        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-        if (!wait_phase(ctl, &ctl->empty[s], ph ^ 1u, status)) {
+        const uint32_t s = it % G::STAGES, ph = (it / G::STAGES) & 1u;
+        if (!wait_phase<CG>(ctl, &ctl->empty[s], ph ^ 1u, status)) {
           ok = false;
           break;
         }
-        uint8_t* a_dst = smem + s * STAGE_BYTES;
+        uint8_t* a_dst = smem + s * G::STAGE_BYTES;
         uint8_t* b_dst = a_dst + A_BYTES;
-        mbar_arrive_expect_tx(&ctl->full[s], STAGE_BYTES);  // paired: half of B comes from the peer
-        load_operand(t.a, &ctl->full[s], a_dst, BM, kb);
-        if constexpr (kPair)
-          load_b_half(t.b, &ctl->full[s], b_dst, kb, rank);
-        else
-          load_operand(t.b, &ctl->full[s], b_dst, BN, kb);
+        // the even CTA's full barrier counts both CTAs' bytes; only the even CTA arrives on it
+        if (rank == 0) mbar_arrive_expect_tx(&ctl->full[s], G::TX_BYTES);
+        const uint32_t bar = CG == 2 ? mapa_u32(smem_u32(&ctl->full[s]), 0) : smem_u32(&ctl->full[s]);
+        load_operand<CG>(t.a, bar, a_dst, BM, kb);
+        load_operand<CG>(t.b, bar, b_dst, G::B_ROWS, kb);
       }
     }
   }
-  if (!ok) {
-    // let the loads already issued land before the CTA can exit
-    const uint32_t first = it > STAGES ? it - STAGES : 0;
-    for (uint32_t k = first; k < it; ++k) drain_phase(&ctl->full[k % STAGES], (k / STAGES) & 1u);
+  if (!ok && rank == 0) {
+    // let the loads already issued land before the CTA can exit (in a pair the even CTA's barrier
+    // also counts the odd CTA's loads)
+    const uint32_t first = it > G::STAGES ? it - G::STAGES : 0;
+    for (uint32_t k = first; k < it; ++k) drain_phase(&ctl->full[k % G::STAGES], (k / G::STAGES) & 1u);
   }
 }
 
-// ---------------------------------------------------------------- MMA issuer (one thread)
-template <bool kPair, class Sched>
+// ---------------------------------------------------------------- MMA issuer (one thread; the even CTA's in a pair)
+template <int CG>
+__device__ __forceinline__ void commit_both(uint64_t* bar) {
+  if constexpr (CG == 2) {
+    umma_commit_cg2(smem_u32(bar));
+    umma_commit_cg2(mapa_u32(smem_u32(bar), 1));
+  } else {
+    umma_commit(bar);
+  }
+}
+
+template <int CG, class Sched>
 __device__ void mma_role(const Sched& sched, const Feed& feed, uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base,
                          int32_t* status) {
+  using G = Geo<CG>;
   uint32_t it = 0, tcount = 0;
   bool ok = true;
   const uint32_t smem0 = smem_u32(smem);
   for (uint32_t i = 0; ok; ++i) {
-    const int u = feed_consume(feed, ctl, i, status, false);
+    const int u = feed_consume<CG>(feed, ctl, i, status, false, 0);
     if (u < 0) break;
     const int len = sched.unit_len(u);
     for (int j = 0; ok && j < len; ++j) {
@@ -298,40 +382,42 @@ __device__ void mma_role(const Sched& sched, const Feed& feed, uint8_t* smem, Sm
       if (t.kblocks == 0) continue;  // empty tile: no accumulator (the epilogue knows)
       const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
       ++tcount;
-      if (!wait_phase(ctl, &ctl->acc_empty[buf], aph ^ 1u, status)) {
+      if (!wait_phase<CG>(ctl, &ctl->acc_empty[buf], aph ^ 1u, status)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
-      const uint32_t idesc = make_idesc_bf16(BM, BN, t.a.mn_major != 0, t.b.mn_major != 0);
+      const uint32_t idesc = make_idesc_bf16(BM * CG, BN, t.a.mn_major != 0, t.b.mn_major != 0);
       for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
-        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-        if (!wait_phase(ctl, &ctl->full[s], ph, status)) {
+        const uint32_t s = it % G::STAGES, ph = (it / G::STAGES) & 1u;
+        if (!wait_phase<CG>(ctl, &ctl->full[s], ph, status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t a_base = smem0 + s * STAGE_BYTES;
+        const uint32_t a_base = smem0 + s * G::STAGE_BYTES;
         const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-          umma_bf16(d_tmem, operand_desc(a_base, t.a.mn_major != 0, kk), operand_desc(b_base, t.b.mn_major != 0, kk), idesc,
-                    (kb | kk) != 0 ? 1u : 0u);
+          const uint64_t ad = operand_desc(a_base, t.a.mn_major != 0, kk);
+          const uint64_t bd = operand_desc(b_base, t.b.mn_major != 0, kk);
+          if constexpr (CG == 2)
+            umma_bf16_cg2(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          else
+            umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
         }
-        // frees the stage once these MMAs have read it (paired: in both CTAs, whose producers
-        // write halves of B into each other's stage)
-        if constexpr (kPair)
-          umma_commit_mc(&ctl->empty[s], 0x3);
-        else
-          umma_commit(&ctl->empty[s]);
+        commit_both<CG>(&ctl->empty[s]);  // frees the stage (in both CTAs) once these MMAs have read it
       }
       if (!ok) break;
-      umma_commit(&ctl->acc_full[buf]);  // accumulator ready for the epilogue
+      commit_both<CG>(&ctl->acc_full[buf]);  // accumulator ready for the epilogue warps (of both CTAs)
     }
   }
   // make sure every issued MMA has finished before TMEM is released
-  umma_commit(&ctl->drain);
+  if constexpr (CG == 2)
+    umma_commit_cg2(smem_u32(&ctl->drain));
+  else
+    umma_commit(&ctl->drain);
   drain_phase(&ctl->drain, 0);
 }
 
@@ -339,19 +425,22 @@ __device__ void mma_role(const Sched& sched, const Feed& feed, uint8_t* smem, Sm
 
 // Waits until accumulator tile `tcount` is ready; returns its TMEM address for
 // this warp's 32 lanes (column 0 of the tile).
+template <int CG = 1>
 __device__ __forceinline__ bool epi_acquire(SmemCtl* ctl, uint32_t tmem_base, uint32_t tcount, int warp,
                                             int32_t* status, uint32_t* taddr) {
   const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
-  if (!wait_phase(ctl, &ctl->acc_full[buf], aph, status)) return false;
+  if (!wait_phase<CG>(ctl, &ctl->acc_full[buf], aph, status)) return false;
   tc_fence_after();
   *taddr = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + buf * BN;
   return true;
 }
 
-__device__ __forceinline__ void epi_release(SmemCtl* ctl, uint32_t tcount) {
+// The accumulator's counter lives in the even CTA: the odd CTA's warps arrive on it remotely.
+template <int CG = 1>
+__device__ __forceinline__ void epi_release(SmemCtl* ctl, uint32_t tcount, uint32_t rank = 0) {
   tc_fence_before();
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl->acc_empty[tcount & 1u]);
+  if ((threadIdx.x & 31) == 0) arrive_leader<CG>(&ctl->acc_empty[tcount & 1u], rank);
 }
 
 // 32 fp32 values of one row -> 128-byte swizzled row `lane` of a 32 x 128 B staging box
@@ -374,55 +463,109 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t box, int lane, const uin
 
 // ---------------------------------------------------------------- CTA driver
 
-// Runs the three roles; `epilogue(smem, ctl, tmem_base, warp, lane)` is the kernel's epilogue loop,
-// which walks the units with feed_consume(feed, ctl, i, status, true).
-template <bool kPair = false, class Sched, class EpiFn>
+// Runs the three roles; `epilogue(staging, ctl, tmem_base, warp, lane, rank)` is the kernel's
+// epilogue loop (`staging` is the base of the epilogue warps' staging boxes, STAGING_PER_WARP bytes
+// per warp), which walks the units with feed_consume<CG>(feed, ctl, i, status, true, rank).
+// CG = 2 must run in 2-CTA clusters.
+template <int CG, class Sched, class EpiFn>
 __device__ __forceinline__ void run_cta(const Sched& sched, const Feed& feed, int32_t* status, EpiFn&& epilogue) {
+  using G = Geo<CG>;
   uint8_t* smem = smem_base_aligned();
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + SMEM_CTL_OFF);
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + G::CTL_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = pair_rank<CG>();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < G::STAGES; ++s) {
       mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], kPair ? 2 : 1);
+      mbar_init(&ctl->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->acc_full[b], 1);
-      mbar_init(&ctl->acc_empty[b], EPI_WARPS);
+      mbar_init(&ctl->acc_empty[b], CG * EPI_WARPS);  // pair: both CTAs' epilogue warps
     }
     mbar_init(&ctl->drain, 1);
     for (int r = 0; r < RING; ++r) {
       mbar_init(&ctl->unit_full[r], 1);
-      mbar_init(&ctl->unit_empty[r], 1 + EPI_WARPS);
+      // MMA thread + epilogue warps; pair: + the odd CTA's producer and epilogue warps
+      mbar_init(&ctl->unit_empty[r], CG == 2 ? 2 + 2 * EPI_WARPS : 1 + EPI_WARPS);
     }
     ctl->abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&ctl->tmem_base, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<CG>(&ctl->tmem_base, TMEM_COLS);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (kPair) cluster_sync();  // the peer's barriers exist before any multicast reaches them
+  if constexpr (CG == 2) cluster_sync();  // the other CTA's barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer_role<kPair>(sched, feed, smem, ctl, status);
+    if (lane == 0) producer_role<CG>(sched, feed, smem, ctl, status, rank);
   } else if (warp == 1) {
-    if (lane == 0) mma_role<kPair>(sched, feed, smem, ctl, tmem_base, status);
+    if (lane == 0 && rank == 0) mma_role<CG>(sched, feed, smem, ctl, tmem_base, status);
   } else {
-    epilogue(smem, ctl, tmem_base, warp, lane);
+    epilogue(smem + G::STAGING_OFF, ctl, tmem_base, warp, lane, rank);
   }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if constexpr (kPair) cluster_sync();  // no CTA leaves while its peer may still write into it
+  // pair: the even CTA's MMAs read the odd CTA's shared memory and write its tensor memory, so neither
+  // leaves (or frees its columns) before both are done
+  if constexpr (CG == 2) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc<CG>(tmem_base, TMEM_COLS);
   }
+}
+
+// ---------------------------------------------------------------- host: launches
+
+// Launches an engine kernel of CTA group `cg`: CG = 2 kernels run as 2-CTA clusters, `grid` counting
+// CTAs (even).
+template <class... Params, class... Args>
+inline cudaError_t launch_engine(void (*kernel)(Params...), int cg, int grid, uint32_t smem, cudaStream_t st,
+                                 Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cg;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cg == 2 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
+// Number of 2-CTA clusters of `kernel` (one CTA per SM) that fit on the current device at once; 0 when
+// none can run.
+template <class Kernel>
+inline int max_pair_clusters(Kernel kernel, uint32_t smem) {
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = 0;
+  cudaGetLastError();
+  return n;
 }
 
 }  // namespace orpo

@@ -21,34 +21,40 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ================================================================ recompute -> S
+// Unit = (M unit, vocabulary tile): an M unit is one row tile (CG = 1) or a pair's two row tiles
+// (CG = 2, CTA rank r taking tile 2m + r; the pair shares the W tile, half fetched by each CTA).
+template <int CG>
 struct RecSched {
   const CUtensorMap* mh;
   const CUtensorMap* mw;
   int m0, v0, n_mt, n_vt, kblocks;
   int w_row0;        // row of the W map that holds vocabulary column v0
-  const int* list;   // backward skips: the tiles to compute (vt * n_mt + mt, in unit order), or nullptr
+  const int* list;   // backward skips (CG = 1): the tiles to compute (vt * n_mt + mt, in unit order), or nullptr
   const int* count;  // number of entries of list
-  int chunk;         // row tiles per L2 chunk (chunk_decode)
+  int chunk;         // M units per L2 chunk (chunk_decode)
   int32_t* status = nullptr;
-  __device__ int num_units() const { return list ? __ldg(count) : n_mt * n_vt; }
+  int rank = 0;      // this CTA's rank in its pair (0 for CG = 1)
+  __device__ int n_mu() const { return (n_mt + CG - 1) / CG; }
+  __device__ int num_units() const { return list ? __ldg(count) : n_mu() * n_vt; }
+  // unit u -> x = vt * n_mu + mu
   __device__ int tile_index(int u) const {
     int x;
     if (list) {
       x = in_bounds(status, u, kMaxTiles) ? __ldg(list + u) : 0;
     } else {
-      int mt, vt;
-      chunk_decode(u, n_mt, n_vt, chunk, mt, vt);
-      x = vt * n_mt + mt;
+      int mu, vt;
+      chunk_decode(u, n_mu(), n_vt, chunk, mu, vt);
+      x = vt * n_mu() + mu;
     }
-    return in_bounds(status, x, n_mt * n_vt) ? x : 0;
+    return in_bounds(status, x, n_mu() * n_vt) ? x : 0;
   }
   __device__ int unit_len(int) const { return 1; }
   __device__ TileOps tile(int u, int) const {
     const int x = tile_index(u);
-    const int vt = x / n_mt, mt = x - vt * n_mt;
+    const int vt = x / n_mu(), mt = (x - vt * n_mu()) * CG + rank;
     TileOps t;
     t.a = Operand{mh, 0, m0 + mt * BM, 0};
-    t.b = Operand{mw, 0, w_row0 + vt * BN, 0};
+    t.b = Operand{mw, 0, w_row0 + vt * BN + rank * (BN / CG), 0};
     t.kblocks = kblocks;
     return t;
   }
@@ -148,30 +154,40 @@ __device__ __forceinline__ void dz_chunk(const uint32_t (&r)[32], int col0, int 
 // kFilter: the coefficient filter of the backward skips ("Steel flash-CCE — handoff" §E).  A tile
 // is kept (its bits set in rowbits and colbits) when some row with g != 0 has |dZ| >= eps |g|,
 // i.e. an entry of (onehot - p) sech^2 reaches eps; the dh / dW GEMMs read only kept tiles.
-template <int cap, bool kFilter>
+template <int cap, bool kFilter, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     rec_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mw,
-               const __grid_constant__ CUtensorMap ms, RecSched sched, RecArgs p) {
+               const __grid_constant__ CUtensorMap ms, RecSched<CG> sched, RecArgs p) {
+  static_assert(!(kFilter && CG == 2), "the backward skips run on single-CTA tiles");
   sched.mh = &mh;
   sched.mw = &mw;
   sched.status = p.status;
+  sched.rank = (int)pair_rank<CG>();
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&mh);
     tma_prefetch_desc(&mw);
     tma_prefetch_desc(&ms);
   }
   const Feed feed{nullptr, sched.num_units()};
-  run_cta(sched, feed, p.status, [&](uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
+  run_cta<CG>(sched, feed, p.status, [&](uint8_t* stg, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane,
+                                         uint32_t rank) {
     const int q = warp & 3;
-    const uint32_t staging = smem_u32(smem + SMEM_STAGING_OFF + (warp - 2) * STAGING_PER_WARP);
+    uint8_t* stage_ptr = stg + (warp - 2) * STAGING_PER_WARP;
+    const uint32_t staging = smem_u32(stage_ptr);
     const float inv_c = cap != kCapOff ? 1.f / p.softcap : 0.f;
     const float cl2 = p.softcap * kLog2e;
     uint32_t tcount = 0, nstore = 0;
     for (uint32_t i = 0;; ++i, ++tcount) {
-      const int u = feed_consume(feed, ctl, i, p.status, true);
+      const int u = feed_consume<CG>(feed, ctl, i, p.status, true, rank);
       if (u < 0) break;
       const int x = sched.tile_index(u);
-      const int vt = x / sched.n_mt, mt = x - vt * sched.n_mt;
+      const int vt = x / sched.n_mu(), mt = (x - vt * sched.n_mu()) * CG + (int)rank;
+      uint32_t taddr;
+      if (mt >= sched.n_mt) {  // the empty half of a pair whose row-tile count is odd: nothing to store
+        if (!epi_acquire<CG>(ctl, tmem_base, tcount, warp, p.status, &taddr)) break;
+        epi_release<CG>(ctl, tcount, rank);
+        continue;
+      }
       const int srow = mt * BM + 32 * q;  // first scratch row of this warp
       const int row = sched.m0 + srow + lane;
       float gval = 0.f, lse2 = 0.f;
@@ -186,8 +202,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         lse2 = p.lse[row] * kLog2e;
       }
       const bool warp_zero = __all_sync(0xffffffffu, gval == 0.f);
-      uint32_t taddr;
-      if (!epi_acquire(ctl, tmem_base, tcount, warp, p.status, &taddr)) break;
+      if (!epi_acquire<CG>(ctl, tmem_base, tcount, warp, p.status, &taddr)) break;
       const int vcol0 = sched.v0 + vt * BN;  // global vocabulary column of the tile
       float amax = 0.f;                       // largest |dZ| of this row in the tile (filter)
       uint32_t ra[32], rb[32];
@@ -213,13 +228,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&ms, smem + SMEM_STAGING_OFF + (warp - 2) * STAGING_PER_WARP + (nstore & 1u) * BOX_BYTES,
-                       vt * BN + gi * 64, srow);
+          tma_store_2d(&ms, stage_ptr + (nstore & 1u) * BOX_BYTES, vt * BN + gi * 64, srow);
           bulk_commit_group();
         }
         ++nstore;
       }
-      epi_release(ctl, tcount);
+      epi_release<CG>(ctl, tcount, rank);
       if constexpr (kFilter) {
         const bool keep = gval != 0.f && amax >= p.eps * fabsf(gval);
         if (__any_sync(0xffffffffu, keep) && lane == 0) {
@@ -251,10 +265,14 @@ struct GemmClass {
   int kbits_rows;  // bitmaps at kbits
 };
 
+// Unit = (class, M unit, N tile); an M unit is one 128-row output tile (CG = 1) or a pair's two
+// (CG = 2: CTA rank r takes output tile 2m + r and fetches half of the B tile).
+template <int CG>
 struct GemmSched {
   const CUtensorMap* maps[6];
   GemmClass cls[2];
   int32_t* status;
+  int rank = 0;  // this CTA's rank in its pair (0 for CG = 1)
   // constant-index selection keeps the pointer table in registers (no local-memory copy)
   __device__ __forceinline__ const CUtensorMap* map(int i) const {
     switch (i) {
@@ -275,20 +293,24 @@ struct GemmSched {
       c = cls[1];
     return c;
   }
-  __device__ int n0() const { return cls[0].n_mt * cls[0].n_nt; }
-  __device__ int num_units() const { return n0() + cls[1].n_mt * cls[1].n_nt; }
+  __device__ static int n_mu(const GemmClass& c) { return (c.n_mt + CG - 1) / CG; }
+  __device__ int n0() const { return n_mu(cls[0]) * cls[0].n_nt; }
+  __device__ int num_units() const { return n0() + n_mu(cls[1]) * cls[1].n_nt; }
   __device__ int unit_len(int) const { return 1; }
+  // mt: this CTA's output row tile (c.n_mt or more: the empty half of a pair whose tile count is odd)
   __device__ void decode(int u, int& k, int& mt, int& nt) const {
     k = u < n0() ? 0 : 1;
     const int v = k == 0 ? u : u - n0();
     const GemmClass c = pick(k);
+    int mu;
     if (c.mt_major) {
-      mt = v / c.n_nt;
-      nt = v - mt * c.n_nt;
+      mu = v / c.n_nt;
+      nt = v - mu * c.n_nt;
     } else {
-      nt = v / c.n_mt;
-      mt = v - nt * c.n_mt;
+      nt = v / n_mu(c);
+      mu = v - nt * n_mu(c);
     }
+    mt = mu * CG + rank;
   }
   __device__ TileOps tile(int u, int) const {
     int k, mt, nt;
@@ -296,9 +318,9 @@ struct GemmSched {
     const GemmClass c = pick(k);
     TileOps t;
     t.a = Operand{map(c.a_map), c.a_mn, c.a_mn_base + mt * BM, c.a_k_base};
-    t.b = Operand{map(c.b_map), c.b_mn, c.b_mn_base + nt * BN, c.b_k_base};
+    t.b = Operand{map(c.b_map), c.b_mn, c.b_mn_base + nt * BN + rank * (BN / CG), c.b_k_base};
     t.kblocks = c.kblocks;
-    if (c.kbits != nullptr) {
+    if (CG == 1 && c.kbits != nullptr) {
       const int br = in_bounds(status, mt >> c.list_shift, c.kbits_rows) ? mt >> c.list_shift : 0;
       const uint32_t* bits = c.kbits + (size_t)br * c.kwords;
       int n = 0;
@@ -314,10 +336,11 @@ struct GemmSched {
   }
 };
 
+template <int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
                 const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
-                const __grid_constant__ CUtensorMap m4, const __grid_constant__ CUtensorMap m5, GemmSched sched,
+                const __grid_constant__ CUtensorMap m4, const __grid_constant__ CUtensorMap m5, GemmSched<CG> sched,
                 int* counter, int32_t* status) {
   sched.maps[0] = &m0;
   sched.maps[1] = &m1;
@@ -326,17 +349,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   sched.maps[4] = &m4;
   sched.maps[5] = &m5;
   sched.status = status;
+  sched.rank = (int)pair_rank<CG>();
   if (threadIdx.x == 0) {
     for (int i = 0; i < 6; ++i) tma_prefetch_desc(sched.maps[i]);
   }
   const Feed feed{counter, sched.num_units()};
-  run_cta(sched, feed, status, [&](uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
+  run_cta<CG>(sched, feed, status, [&](uint8_t* stg, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane,
+                                       uint32_t rank) {
     const int q = warp & 3;
-    uint8_t* stage_ptr = smem + SMEM_STAGING_OFF + (warp - 2) * STAGING_PER_WARP;
+    uint8_t* stage_ptr = stg + (warp - 2) * STAGING_PER_WARP;
     const uint32_t staging = smem_u32(stage_ptr);
     uint32_t tcount = 0, nstore = 0;
     for (uint32_t i = 0;; ++i) {
-      const int u = feed_consume(feed, ctl, i, status, true);
+      const int u = feed_consume<CG>(feed, ctl, i, status, true, rank);
       if (u < 0) break;
       int k, mt, nt;
       sched.decode(u, k, mt, nt);
@@ -344,7 +369,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const CUtensorMap* out = sched.map(c.out_map);
       const int orow = c.out_row_base + mt * BM + 32 * q;
       const int ocol0 = c.out_col_base + nt * BN;
-      if (sched.tile(u, 0).kblocks == 0) {
+      if (CG == 1 && sched.tile(u, 0).kblocks == 0) {
         // empty sparse tile: nothing to add; a first (store) write still owes the tile its zeros
         if (!c.reduce && orow < c.out_rows) {
 #pragma unroll 1
@@ -368,8 +393,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         continue;
       }
       uint32_t taddr;
-      if (!epi_acquire(ctl, tmem_base, tcount, warp, status, &taddr)) break;
-      if (orow < c.out_rows) {
+      if (!epi_acquire<CG>(ctl, tmem_base, tcount, warp, status, &taddr)) break;
+      if (mt < c.n_mt && orow < c.out_rows) {  // (the empty half of an odd pair stores nothing)
         uint32_t ra[32], rb[32];
         tmem_ld32(taddr, ra);
 #pragma unroll 1
@@ -406,7 +431,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      epi_release(ctl, tcount);
+      epi_release<CG>(ctl, tcount, rank);
       ++tcount;
     }
     if (lane == 0) bulk_wait_group<0>();
@@ -417,37 +442,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }  // namespace
 
 namespace {
-template <int cap, bool kFilter>
+template <int cap, bool kFilter, int CG>
 cudaError_t launch_rec_kernel(const RecLaunch& L, cudaStream_t st) {
   static std::atomic<int> smem_set[64];
-  if (cudaError_t e = opt_in_smem(rec_kernel<cap, kFilter>, SMEM_TOTAL, smem_set)) return e;
-  const int chunk = L.chunk > 0 && L.chunk < L.n_mt ? L.chunk : L.n_mt;
-  RecSched sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks, L.w_row0, L.list, L.count, chunk};
+  if (cudaError_t e = opt_in_smem(rec_kernel<cap, kFilter, CG>, Geo<CG>::SMEM, smem_set)) return e;
+  const int n_mu = (L.n_mt + CG - 1) / CG;
+  const int chunk = L.chunk > 0 && L.chunk < n_mu ? L.chunk : n_mu;
+  RecSched<CG> sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks, L.w_row0, L.list, L.count, chunk};
   RecArgs a{L.targets, L.mask, L.lse, L.g, L.M, L.V, L.softcap, L.status, L.eps, L.rowbits, L.colbits, L.ld_row,
             L.ld_col};
   prof_begin(K_REC, st);
-  rec_kernel<cap, kFilter><<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, L.ms_store, sched, a);
+  const cudaError_t e =
+      launch_engine(rec_kernel<cap, kFilter, CG>, CG, L.grid, Geo<CG>::SMEM, st, L.mh, L.mw, L.ms_store, sched, a);
   prof_end(K_REC, st);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <bool kFilter>
+template <bool kFilter, int CG>
 cudaError_t launch_rec_cap(const RecLaunch& L, cudaStream_t st) {
   const int cap = L.softcap > 0.f ? (L.softcap <= kCapExpMax ? kCapExp : kCapHybrid) : kCapOff;
-  return cap == kCapExp      ? launch_rec_kernel<kCapExp, kFilter>(L, st)
-         : cap == kCapHybrid ? launch_rec_kernel<kCapHybrid, kFilter>(L, st)
-                             : launch_rec_kernel<kCapOff, kFilter>(L, st);
-}
-}  // namespace
-
-cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st) {
-  return L.rowbits ? launch_rec_cap<true>(L, st) : launch_rec_cap<false>(L, st);
+  return cap == kCapExp      ? launch_rec_kernel<kCapExp, kFilter, CG>(L, st)
+         : cap == kCapHybrid ? launch_rec_kernel<kCapHybrid, kFilter, CG>(L, st)
+                             : launch_rec_kernel<kCapOff, kFilter, CG>(L, st);
 }
 
-cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
+template <int CG>
+cudaError_t launch_gemm_cg(const GemmLaunch& L, cudaStream_t st, int kind) {
   static std::atomic<int> smem_set[64];
-  if (cudaError_t e = opt_in_smem(gemm_kernel, SMEM_TOTAL, smem_set)) return e;
-  GemmSched sched;
+  if (cudaError_t e = opt_in_smem(gemm_kernel<CG>, Geo<CG>::SMEM, smem_set)) return e;
+  GemmSched<CG> sched;
   for (int i = 0; i < 6; ++i) sched.maps[i] = nullptr;
   sched.status = nullptr;
   for (int k = 0; k < 2; ++k) {
@@ -459,10 +482,20 @@ cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
                              h.kbits_rows};
   }
   prof_begin(kind, st);
-  gemm_kernel<<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.maps[0], L.maps[1], L.maps[2], L.maps[3], L.maps[4],
-                                                       L.maps[5], sched, L.counter, L.status);
+  const cudaError_t e = launch_engine(gemm_kernel<CG>, CG, L.grid, Geo<CG>::SMEM, st, L.maps[0], L.maps[1], L.maps[2],
+                                      L.maps[3], L.maps[4], L.maps[5], sched, L.counter, L.status);
   prof_end(kind, st);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st) {
+  if (L.rowbits) return launch_rec_cap<true, 1>(L, st);
+  return L.cg == 2 ? launch_rec_cap<false, 2>(L, st) : launch_rec_cap<false, 1>(L, st);
+}
+
+cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
+  return L.cg == 2 ? launch_gemm_cg<2>(L, st, kind) : launch_gemm_cg<1>(L, st, kind);
 }
 
 }  // namespace orpo

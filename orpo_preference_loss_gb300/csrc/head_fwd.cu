@@ -11,6 +11,8 @@
 // in base-2 units and captures the target logit.  At the end of the unit the
 // row's partial (max, sum) is written to the workspace; a small merge kernel
 // combines the splits into lse and logp.
+#include <stdlib.h>
+
 #include "engine.cuh"
 #include "internal.h"
 
@@ -21,26 +23,28 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Pair mode: the CTAs of a 2-CTA cluster take row tiles 2p and 2p + 1 of the same split, walk the
-// same vocabulary tiles in lockstep, and each fetches half of every W tile for both (TMA multicast),
-// so W crosses from L2 to the SMs once per pair of row tiles instead of once per row tile.
+// Unit = (M unit, split), where an M unit is one row tile (CG = 1) or the two row tiles of a 2-CTA
+// pair (CG = 2; CTA rank r takes tile 2m + r, and the W tiles of the split are shared by the pair).
+// Units are ordered split-major within L2 chunks of M units, so the CTAs running at the same time
+// stream the same W split through L2.
+template <int CG>
 struct FwdSched {
   const CUtensorMap* mh;
   const CUtensorMap* mw;
-  int n_mt, nsplit, n_vt, kblocks;  // pair mode: n_mt is even
-  int chunk;                        // units along M per L2 chunk (chunk_decode)
-  int pair, rank;                   // pair mode flag; this CTA's rank in its cluster (0 otherwise)
-  __device__ int n_mu() const { return pair ? n_mt >> 1 : n_mt; }
+  int n_mt, nsplit, n_vt, kblocks;
+  int chunk;  // M units per L2 chunk (chunk_decode)
+  int rank;   // this CTA's rank in its pair (0 for CG = 1)
+  __device__ int n_mu() const { return (n_mt + CG - 1) / CG; }
   __device__ int num_units() const { return n_mu() * nsplit; }
   __device__ int split_of(int u) const {
     int m, s;
     chunk_decode(u, n_mu(), nsplit, chunk, m, s);
     return s;
   }
-  __device__ int mt_of(int u) const {
+  __device__ int mt_of(int u) const {  // this CTA's row tile (n_mt itself: the empty half of an odd pair)
     int m, s;
     chunk_decode(u, n_mu(), nsplit, chunk, m, s);
-    return pair ? 2 * m + rank : m;
+    return m * CG + rank;
   }
   __device__ int vt_begin(int s) const { return (int)(((long long)s * n_vt) / nsplit); }
   __device__ int unit_len(int u) const {
@@ -52,7 +56,7 @@ struct FwdSched {
     const int vt = vt_begin(s) + j;
     TileOps t;
     t.a = Operand{mh, 0, mt * BM, 0};
-    t.b = Operand{mw, 0, vt * BN, 0};
+    t.b = Operand{mw, 0, vt * BN + rank * (BN / CG), 0};  // a pair fetches one half of the W tile each
     t.kblocks = kblocks;
     return t;
   }
@@ -158,28 +162,26 @@ __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, in
   st.m = mnew;
 }
 
-template <int cap, bool kPair>
+template <int cap, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    fwd_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mw, FwdSched sched,
+    fwd_kernel(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mw, FwdSched<CG> sched,
                FwdArgs p) {
   sched.mh = &mh;
   sched.mw = &mw;
-  sched.pair = kPair ? 1 : 0;
-  sched.rank = kPair ? (int)cluster_ctarank() : 0;
+  sched.rank = (int)pair_rank<CG>();
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&mh);
     tma_prefetch_desc(&mw);
   }
-  // pair mode: cluster c takes pair units c, c + C, ... (C clusters; 1-D grid, rank = blockIdx.x % 2)
-  const Feed feed = kPair ? Feed{nullptr, sched.num_units(), (int)(blockIdx.x >> 1), (int)(gridDim.x >> 1)}
-                          : Feed{nullptr, sched.num_units()};
-  run_cta<kPair>(sched, feed, p.status, [&](uint8_t*, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane) {
+  const Feed feed{nullptr, sched.num_units()};
+  run_cta<CG>(sched, feed, p.status, [&](uint8_t*, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane,
+                                         uint32_t rank) {
     const int q = warp & 3;
     const float inv_c = cap != kCapOff ? 1.f / p.softcap : 0.f;
     const float cl2 = p.softcap * kLog2e;
     uint32_t tcount = 0;
     for (uint32_t i = 0;; ++i) {
-      const int u = feed_consume(feed, ctl, i, p.status, true);
+      const int u = feed_consume<CG>(feed, ctl, i, p.status, true, rank);
       if (u < 0) break;
       const int s = sched.split_of(u), mt = sched.mt_of(u);
       const int row = mt * BM + 32 * q + lane;
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int vt0 = sched.vt_begin(s);
       for (int j = 0; j < len; ++j, ++tcount) {
         uint32_t taddr;
-        if (!epi_acquire(ctl, tmem_base, tcount, warp, p.status, &taddr)) return;
+        if (!epi_acquire<CG>(ctl, tmem_base, tcount, warp, p.status, &taddr)) return;
         const int col_base = p.col0 + (vt0 + j) * BN;
         uint32_t ra[32], rb[32];
         float tmax = -INFINITY;
@@ -207,7 +209,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (c + 2 < BN / 32) tmem_ld32(taddr + (c + 2) * 32, ra);
           fold_chunk<cap>(rb, col_base + (c + 1) * 32, p.V, y, inv_c, cl2, st, tgt_slot, tmax);
         }
-        epi_release(ctl, tcount);
+        epi_release<CG>(ctl, tcount, rank);
         if (p.bmax != nullptr) {
           float v = supervised ? tmax : -INFINITY;
 #pragma unroll
@@ -216,8 +218,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             p.bmax[(size_t)grp * p.bmax_ld + col_base / BN] = v;
         }
       }
-      if (row < p.Mpad && in_bounds(p.status, p.split0 + s, p.part_cap)) {  // pair mode pads an odd
-        p.part_m[(size_t)(p.split0 + s) * p.Mpad + row] = st.m;                // tile count with an empty tile
+      if (row < p.Mpad && in_bounds(p.status, p.split0 + s, p.part_cap)) {
+        p.part_m[(size_t)(p.split0 + s) * p.Mpad + row] = st.m;
         p.part_s[(size_t)(p.split0 + s) * p.Mpad + row] = st.s;
       }
     }
@@ -251,78 +253,56 @@ __global__ void merge_kernel(const float* __restrict__ part_m, const float* __re
   if (err) atomicOr(status, err);
 }
 
-template <int cap, bool kPair>
+template <int cap, int CG>
 cudaError_t launch_fwd_kernel(const FwdLaunch& L, cudaStream_t st) {
   static std::atomic<int> smem_set[64];
-  if (cudaError_t e = opt_in_smem(fwd_kernel<cap, kPair>, SMEM_TOTAL, smem_set)) return e;
-  const int n_mt = kPair ? (L.n_mt + 1) & ~1 : L.n_mt;
-  const int n_mu = kPair ? n_mt / 2 : n_mt;
+  if (cudaError_t e = opt_in_smem(fwd_kernel<cap, CG>, Geo<CG>::SMEM, smem_set)) return e;
+  const int n_mu = (L.n_mt + CG - 1) / CG;
   const int chunk = L.chunk > 0 && L.chunk < n_mu ? L.chunk : n_mu;
-  FwdSched sched{nullptr, nullptr, n_mt, L.nsplit, L.n_vt, L.kblocks, chunk, 0, 0};
+  FwdSched<CG> sched{nullptr, nullptr, L.n_mt, L.nsplit, L.n_vt, L.kblocks, chunk, 0};
   FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M,      L.Mpad,
             L.V,       L.softcap, L.status, L.col0, L.split0, L.bmax, (L.V + BN - 1) / BN, L.part_cap};
-  cudaError_t e = cudaSuccess;
   prof_begin(K_FWD, st);
-  if constexpr (kPair) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)L.grid);
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = SMEM_TOTAL;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fwd_kernel<cap, true>, L.mh, L.mw, sched, a);
-  } else {
-    fwd_kernel<cap, false><<<L.grid, NUM_THREADS, SMEM_TOTAL, st>>>(L.mh, L.mw, sched, a);
-  }
+  const cudaError_t e = launch_engine(fwd_kernel<cap, CG>, CG, L.grid, Geo<CG>::SMEM, st, L.mh, L.mw, sched, a);
   prof_end(K_FWD, st);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <bool kPair>
-cudaError_t launch_fwd_cap(const FwdLaunch& L, cudaStream_t st) {
+template <int CG>
+cudaError_t launch_fwd_cg(const FwdLaunch& L, cudaStream_t st) {
   const int cap = L.softcap > 0.f ? (L.softcap <= kCapExpMax ? kCapExp : kCapHybrid) : kCapOff;
-  return cap == kCapExp      ? launch_fwd_kernel<kCapExp, kPair>(L, st)
-         : cap == kCapHybrid ? launch_fwd_kernel<kCapHybrid, kPair>(L, st)
-                             : launch_fwd_kernel<kCapOff, kPair>(L, st);
+  return cap == kCapExp      ? launch_fwd_kernel<kCapExp, CG>(L, st)
+         : cap == kCapHybrid ? launch_fwd_kernel<kCapHybrid, CG>(L, st)
+                             : launch_fwd_kernel<kCapOff, CG>(L, st);
 }
 
 }  // namespace
 
-int forward_pair_clusters() {
-  static std::atomic<int> cached[64];  // 0 unknown, -1 unavailable, else the cluster count
+// Looked up once per device.
+int engine_pair_clusters() {
+  static std::atomic<int> cached[64];  // 0 unknown, -1 none, else the cluster count
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   const int c = cached[dev].load(std::memory_order_acquire);
   if (c != 0) return c > 0 ? c : 0;
-  static std::atomic<int> smem_set[64];
-  int n = 0;
-  if (opt_in_smem(fwd_kernel<kCapExp, true>, SMEM_TOTAL, smem_set) == cudaSuccess) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = SMEM_TOTAL;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, fwd_kernel<kCapExp, true>, &cfg) != cudaSuccess) n = 0;
-  }
-  cudaGetLastError();
+  const int n = max_pair_clusters(fwd_kernel<kCapExp, 2>, Geo<2>::SMEM);
   cached[dev].store(n > 0 ? n : -1, std::memory_order_release);
   return n > 0 ? n : 0;
 }
 
+// Read once per process: ORPO_CTA_GROUP=1 runs every engine kernel on single-CTA tiles, =2 every
+// one on 2-CTA clusters; otherwise only the dh / dW GEMM uses clusters.
+int engine_cta_group_override() {
+  static const int v = [] {
+    const char* env = getenv("ORPO_CTA_GROUP");
+    if (env != nullptr && (env[0] == '1' || env[0] == '2') && env[1] == 0) return env[0] - '0';
+    return 0;
+  }();
+  return v;
+}
+
 cudaError_t launch_forward_logits(const FwdLaunch& L, cudaStream_t st) {
-  return L.pair ? launch_fwd_cap<true>(L, st) : launch_fwd_cap<false>(L, st);
+  return L.cg == 2 ? launch_fwd_cg<2>(L, st) : launch_fwd_cg<1>(L, st);
 }
 
 cudaError_t launch_forward_merge(const FwdLaunch& L, int nsplit_total, cudaStream_t st) {

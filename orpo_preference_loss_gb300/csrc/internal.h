@@ -36,7 +36,7 @@ constexpr int64_t kScratchBudget = 256ll << 20;  // bytes of the bf16 dZ block
 constexpr int kMaxTiles = (int)(kScratchBudget / 2 / (kBM * kBN));  // 128 x 256 tiles in one dZ block
 
 // ---- L2-aware unit order (chunk_decode in engine.cuh): units along M per chunk.  The rows of h
-// that concurrently running units re-read (one 128-row tile, or a pair, per M unit) are kept within
+// that concurrently running units re-read (one 128-row tile per M unit) are kept within
 // kL2ChunkBytes; the chunks are then made about equal.
 constexpr int64_t kL2ChunkBytes = 48ll << 20;
 __host__ __device__ inline int l2_chunk(int n_m, int64_t bytes_per_m) {
@@ -46,9 +46,17 @@ __host__ __device__ inline int l2_chunk(int n_m, int64_t bytes_per_m) {
   return (int)((n_m + nc - 1) / nc);
 }
 
+// ---- tensor-core CTA group of the engine kernels (engine.cuh): 2 = 2-CTA clusters sharing each
+// tcgen05.mma, 1 = single-CTA tiles.  The host encodes the B operand's tensor map with boxes of
+// kBN / cg rows (each CTA of a pair fetches half of B).  By default the dh / dW GEMM runs on
+// clusters (where they fit) and the forward and the recompute on single CTAs, the faster choice
+// for each in the power-capped step; ORPO_CTA_GROUP=1 or =2 forces one form everywhere.
+int engine_pair_clusters();       // co-resident 2-CTA clusters on the current device (0: none)
+int engine_cta_group_override();  // 0 (default policy), 1 or 2 (ORPO_CTA_GROUP)
+
 // ---- forward
 struct FwdLaunch {
-  CUtensorMap mh, mw;  // h K-major box {64,128}; W K-major box {64,256}
+  CUtensorMap mh, mw;  // h K-major box {64,128}; W K-major box {64,256 / cg}
   int n_mt, nsplit, n_vt, kblocks;
   const int32_t* targets;
   const uint8_t* mask;
@@ -63,18 +71,17 @@ struct FwdLaunch {
   int col0 = 0;    // vocabulary column of row 0 of mw
   int split0 = 0;  // first split index this launch writes
   int part_cap = 0;  // splits part_m / part_s hold (Mpad floats each)
-  int pair = 0;    // 1: 2-CTA clusters share W tiles (mw box {64,128}; grid = 2 x clusters; n_mt padded to even)
   float* bmax = nullptr;  // optional block maxima [ceil(M/32), ceil(V/256)] (base-2 softcapped logits)
-  int chunk = 0;          // M units per L2 chunk (l2_chunk); 0: all of them
+  int chunk = 0;          // M units (row tiles, or pairs of them) per L2 chunk (l2_chunk); 0: all of them
+  int cg = 1;             // CTA group; grid = cg x (CTAs or clusters)
 };
-int forward_pair_clusters();  // co-resident 2-CTA clusters of the forward kernel (0: pair mode unavailable)
 cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st);  // logits kernel + merge of L.nsplit splits
 cudaError_t launch_forward_logits(const FwdLaunch& L, cudaStream_t st);
 cudaError_t launch_forward_merge(const FwdLaunch& L, int nsplit_total, cudaStream_t st);
 
 // ---- backward: recompute dZ for one (row block, vocab block) into the scratch
 struct RecLaunch {
-  CUtensorMap mh, mw, ms_store;  // h, W as in the forward; S store box {64,32}
+  CUtensorMap mh, mw, ms_store;  // h, W as in the forward (W box {64, 256 / cg}); S store box {64,32}
   int m0, v0, n_mt, n_vt, kblocks;
   const int32_t* targets;
   const uint8_t* mask;
@@ -92,7 +99,8 @@ struct RecLaunch {
   uint32_t* colbits = nullptr;  // or nullptr for no filter
   int ld_row = 0, ld_col = 0;
   float eps = 0.f;
-  int chunk = 0;                // row tiles per L2 chunk (l2_chunk); 0: all of them
+  int chunk = 0;                // M units per L2 chunk (l2_chunk); 0: all of them
+  int cg = 1;                   // CTA group (1 whenever the skip bitmaps or lists are used)
 };
 cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st);
 
@@ -150,11 +158,12 @@ struct GemmClassH {
   int kbits_rows = 0;  // bitmaps at kbits (bounds-checked build)
 };
 struct GemmLaunch {
-  CUtensorMap maps[6];
-  GemmClassH cls[2];
+  CUtensorMap maps[6];   // B operands' boxes cover kBN / cg rows or columns
+  GemmClassH cls[2];     // n_mt counts 128-row output tiles; a pair takes two
   int* counter;  // zeroed unit counter (dynamic scheduling), or nullptr for static round-robin
   int32_t* status;
   int grid;
+  int cg = 1;    // CTA group (1 whenever a class has sparse K)
 };
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind);
 
