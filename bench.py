@@ -90,11 +90,12 @@ def workload_config(w):
 L2_BYTES = 126 << 20  # GB300 L2
 
 
-# device code each kernel kind is built from (its DRAM-traffic figure is void once any of these changes)
+# code each kernel kind's traffic depends on: its device code, and the host code that sets its blocking
+# and launch shape (its DRAM-traffic figure is void once any of these changes)
 KERNEL_SOURCES = {
-    "fwd_logits": ("head_fwd.cu", "engine.cuh", "ptx.cuh"),
-    "bwd_recompute": ("head_bwd.cu", "engine.cuh", "ptx.cuh"),
-    "bwd_grad_gemm": ("head_bwd.cu", "engine.cuh", "ptx.cuh"),
+    "fwd_logits": ("head_fwd.cu", "engine.cuh", "ptx.cuh", "api.cu", "internal.h"),
+    "bwd_recompute": ("head_bwd.cu", "engine.cuh", "ptx.cuh", "api.cu", "internal.h"),
+    "bwd_grad_gemm": ("head_bwd.cu", "engine.cuh", "ptx.cuh", "api.cu", "internal.h"),
 }
 
 
