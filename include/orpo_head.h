@@ -203,10 +203,12 @@ int orpo_head_bwd(const void* h_bf16, const void* W_bf16, const int32_t* targets
  *   scales, biases  bf16 bit patterns [V, d / group];
  *   bits    4 or 8;  group  a multiple of 8 that divides d.
  * The head's weight is W[v, j] = bf16(scales[v, j/group] * q[v, j] + biases[v, j/group])
- * (fp32 arithmetic, one nearest-even rounding).  Each call dequantises W one
- * vocabulary block at a time into the workspace (bounded, at most 256 MiB of bf16)
- * and runs the bf16 tensor-core path on it; nothing grows like V * d beyond the
- * quantised weights themselves.  dW, when given, is the gradient with respect to
+ * (fp32 arithmetic, one nearest-even rounding).  Each call walks W in vocabulary
+ * blocks, dequantised alternately into two bf16 buffers of the workspace (at most
+ * 128 MiB each, unless a single 256-row block is larger): the first block by a
+ * launch of its own, every later one by a spare warp of each tensor-core kernel
+ * while the previous block is multiplied.  The bf16 tensor-core path runs on the
+ * dequantised blocks; nothing grows like V * d beyond the quantised weights.  dW, when given, is the gradient with respect to
  * the dequantised weight.  The workspace must hold orpo_head_q_workspace_bytes.
  * Host errors: ORPO_ERR_ARG for bits / group, ORPO_ERR_ALIGN for wq alignment.
  */

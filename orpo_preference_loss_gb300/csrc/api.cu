@@ -71,18 +71,26 @@ struct BwdBlocks {
   int64_t Mc, Vc;  // rows / columns of the scratch block (multiples of 128 / 256)
 };
 
-// quantised head: the bf16 copy of W is made one vocabulary block at a time within this budget
-constexpr int64_t kWBlockBudget = 256ll << 20;
+// quantised head: the bf16 copy of W is made one vocabulary block at a time, within this many bytes
+// in all.  From kSideMinRows rows on, every block after the first is dequantised by the contraction
+// kernels' spare warps while the previous one is multiplied, so the bytes form two buffers of half
+// the size; below, where a block's contraction is shorter than that dequantisation (about 0.35 ms
+// for a 16384 x 2560 block), each block is dequantised by a launch of its own into one buffer.
+constexpr int64_t kWBudget = 256ll << 20;
+constexpr int64_t kSideMinRows = 8192;
 
-// qd > 0: the quantised head of hidden size qd, whose vocabulary block must also fit the bf16
-// W-block budget (with few rows the dZ budget alone would allow the whole vocabulary, and the
-// dequantised copy would be all of W)
+inline bool q_side(int64_t M) { return M >= kSideMinRows; }
+
+// qd > 0: the quantised head of hidden size qd, whose vocabulary block must also fit one bf16 W
+// buffer (with few rows the dZ budget alone would allow the whole vocabulary, and the dequantised
+// copy would be all of W)
 BwdBlocks bwd_blocks(int64_t M, int64_t V, int64_t qd = 0) {
   const int64_t Mpad = std::max<int64_t>(kBM, cdiv(M, kBM) * kBM);
   const int64_t Mc = std::min(Mpad, kMcMax);
   const int64_t Vpad = cdiv(V, kBN) * kBN;
   int64_t vc = (kScratchBudget / (2 * Mc)) / kBN * kBN;
-  if (qd > 0) vc = std::min<int64_t>(vc, (kWBlockBudget / (2 * qd)) / kBN * kBN);
+  const int64_t wbuf = q_side(M) ? kWBudget / 2 : kWBudget;
+  if (qd > 0) vc = std::min<int64_t>(vc, (wbuf / (2 * qd)) / kBN * kBN);
   vc = std::max<int64_t>(kBN, vc);
   return BwdBlocks{Mc, std::min(Vpad, vc)};
 }
@@ -93,7 +101,7 @@ size_t partial_bytes(int64_t M, int nsplit_max) {
   return (size_t)2 * nsplit_max * Mpad * sizeof(float);
 }
 
-// quantised head: most splits over all dequantised blocks
+// quantised head: most splits over all dequantised blocks (at least one per block; see QLayout)
 constexpr int kNsplitMaxQ = 256;
 
 void* align_ws(void* ws) {
@@ -106,21 +114,10 @@ void* align_ws(void* ws) {
 // same power-of-two address offsets.
 inline int64_t scratch_pitch(const BwdBlocks& b) { return b.Vc + 64; }
 
-size_t scratch_bytes(int64_t M, int64_t V) {
-  const BwdBlocks b = bwd_blocks(M, V);
+size_t scratch_bytes(int64_t M, int64_t V, int64_t qd = 0) {
+  const BwdBlocks b = bwd_blocks(M, V, qd);
   return (size_t)b.Mc * scratch_pitch(b) * 2;
 }
-
-// Rows of W dequantised at a time: a multiple of the backward's vocabulary block (so the backward
-// reuses the same buffer block by block) within kWBlockBudget bytes of bf16, at least one block.
-int64_t wblock_rows(int64_t M, int64_t V, int64_t d) {
-  const BwdBlocks b = bwd_blocks(M, V, d);
-  const int64_t fit = kWBlockBudget / (2 * d);
-  const int64_t k = std::max<int64_t>(1, fit / b.Vc);
-  return std::min(cdiv(V, kBN) * kBN, k * b.Vc);
-}
-
-size_t wblock_bytes(int64_t M, int64_t V, int64_t d) { return (size_t)wblock_rows(M, V, d) * d * 2; }
 
 // Unit counters of the dh/dW GEMM launches (dynamic scheduling): a fixed ring of
 // kCounters slots; launch k uses slot k % kCounters and the ring is zeroed
@@ -231,11 +228,32 @@ int check_quant(const QuantW* q, int64_t d) {
   return ORPO_OK;
 }
 
-// workspace layout (quantised path): [partials | S + counters] then the bf16 W block
-void* wblock_ptr(void* workspace, int64_t M, int64_t V) {
-  uintptr_t p = reinterpret_cast<uintptr_t>(align_ws(workspace));
-  p += std::max(partial_bytes(M, kNsplitMaxQ), scratch_bytes(M, V) + kCounterBytes + kSkipBytes);
-  return reinterpret_cast<void*>((p + 1023) & ~uintptr_t(1023));
+// Quantised head: the forward and the backward walk W in the same vocabulary blocks (the backward's
+// Vc), dequantised alternately into two bf16 buffers (one buffer below kSideMinRows rows).
+// Workspace: [partials | S + counters + skip area], then the buffers.  The forward keeps at least
+// one split per block, so the partials hold max(kNsplitMaxQ, blocks) splits.
+struct QLayout {
+  int64_t rows;     // vocabulary rows per block (= per buffer)
+  int64_t nblocks;  // blocks covering V
+  int nsplit_cap;   // forward splits the partial arrays hold
+  size_t buf_off[2], total;  // one buffer: both offsets equal
+};
+
+QLayout q_layout(int64_t M, int64_t V, int64_t d) {
+  QLayout L{};
+  L.rows = bwd_blocks(M, V, d).Vc;
+  L.nblocks = cdiv(V, L.rows);
+  L.nsplit_cap = (int)std::max<int64_t>(kNsplitMaxQ, L.nblocks);
+  const size_t head = std::max(partial_bytes(M, L.nsplit_cap), scratch_bytes(M, V, d) + kCounterBytes + kSkipBytes);
+  const size_t buf = ((size_t)L.rows * d * 2 + 1023) & ~size_t(1023);
+  L.buf_off[0] = (head + 1023) & ~size_t(1023);
+  L.buf_off[1] = L.buf_off[0] + (q_side(M) ? buf : 0);
+  L.total = L.buf_off[1] + buf + 1024;  // + slack for aligning the workspace base
+  return L;
+}
+
+void* qbuf_ptr(void* workspace, const QLayout& L, int64_t block) {
+  return static_cast<uint8_t*>(align_ws(workspace)) + L.buf_off[block & 1];
 }
 
 int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* targets, const uint8_t* mask,
@@ -256,7 +274,8 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   FwdLaunch L;
   const int64_t n_mt = cdiv(M, kBM);
   const int64_t Mpad = n_mt * kBM;
-  const int nsplit_max = q ? kNsplitMaxQ : kNsplitMax;
+  const QLayout ql = q ? q_layout(M, V, d) : QLayout{};
+  const int nsplit_max = q ? ql.nsplit_cap : kNsplitMax;
   float* base = reinterpret_cast<float*>(align_ws(workspace));
   if (!encode_map_2d(&L.mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, kBM)) return ORPO_ERR_CUDA;
   L.n_mt = (int)n_mt;
@@ -274,24 +293,32 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   L.softcap = softcap > 0.f ? softcap : 0.f;
   L.status = status;
   L.bmax = bmax;
-  // vocabulary blocks: the whole vocabulary for bf16 W; bounded dequantised blocks otherwise
-  const int64_t vb = q ? wblock_rows(M, V, d) : V;
+  // vocabulary blocks: the whole vocabulary for bf16 W; bounded dequantised blocks otherwise.  At
+  // large M block k + 1 is dequantised by the spare warps of block k's launch (only block 0 by a
+  // launch of its own); at small M every block by a launch of its own.
+  const int64_t vb = q ? ql.rows : V;
   const int64_t nblocks = cdiv(V, vb);
   const int per_block = std::max<int>(1, nsplit_max / (int)nblocks);
-  void* Wb = q ? wblock_ptr(workspace, M, V) : nullptr;
+  const bool side = q && q_side(M);
   const Placement pl = placement(sms, false);
   const int64_t n_mu = cdiv(n_mt, pl.cg);  // M units: row tiles, or pairs of them
   L.cg = pl.cg;
   L.chunk = l2_chunk((int)n_mu, (int64_t)pl.cg * kBM * d * 2);
   const uint32_t w_box = kBN / pl.cg;
   int split0 = 0;
-  for (int64_t v0 = 0; v0 < V; v0 += vb) {
+  for (int64_t v0 = 0, blk = 0; v0 < V; v0 += vb, ++blk) {
     const int64_t vc = std::min(vb, V - v0);
     const int64_t n_vt = cdiv(vc, kBN);
     if (q) {
-      if (launch_dequant(q->wq, q->scales, q->biases, q->bits, q->group, v0, vc, d, V, Wb, status, st) != cudaSuccess)
+      if ((blk == 0 || !side) && launch_dequant(q->wq, q->scales, q->biases, q->bits, q->group, v0, vc, d, V,
+                                                qbuf_ptr(workspace, ql, blk), status, st) != cudaSuccess)
         return ORPO_ERR_CUDA;
-      if (!encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Wb, d, vc, d * 2, 64, w_box)) return ORPO_ERR_CUDA;
+      if (!encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qbuf_ptr(workspace, ql, blk), d, vc, d * 2, 64, w_box))
+        return ORPO_ERR_CUDA;
+      const int64_t n0 = v0 + vb;  // the next block, into the other buffer
+      L.side = side && n0 < V ? dequant_job(q->wq, q->scales, q->biases, q->bits, q->group, n0, std::min(vb, V - n0),
+                                            d, V, qbuf_ptr(workspace, ql, blk + 1))
+                              : DequantJob{};
     } else if (!encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, w_box)) {
       return ORPO_ERR_CUDA;
     }
@@ -373,7 +400,7 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
 
   const BwdBlocks B = bwd_blocks(M, V, q ? d : 0);
   void* S = align_ws(workspace);
-  int* counters = reinterpret_cast<int*>(static_cast<uint8_t*>(S) + scratch_bytes(M, V));
+  int* counters = reinterpret_cast<int*>(static_cast<uint8_t*>(S) + scratch_bytes(M, V, q ? d : 0));
   // backward skips: plan rounds over the blocks, slots in the area after the counters
   const bool skip = eps > 0.f;
   SkipPlan P{};
@@ -392,7 +419,7 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
     if ((int64_t)P.shape.n_mt * P.shape.n_vt > kMaxTiles) return ORPO_ERR_SHAPE;  // cannot happen: Mc Vc bounded
     round_slots = (int)std::min<int64_t>(nblocks_all, (int64_t)(kSkipBytes / P.shape.slot_bytes));
   }
-  void* Wb = q ? wblock_ptr(workspace, M, V) : nullptr;
+  const QLayout ql = q ? q_layout(M, V, d) : QLayout{};
   int64_t launch = 0;
   const int64_t sp = scratch_pitch(B);
   // the skips' bitmaps and tile lists are per 128-row tile
@@ -433,14 +460,19 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   R.status = status;
   R.kblocks = (int)cdiv(d, 64);
 
+  // quantised head: vocabulary block 0 is dequantised by a launch of its own; at large M block v + 1
+  // by the spare warps of block v's first recompute (into the other buffer; the block's last GEMM,
+  // which read that buffer's previous block, precedes it on the stream), at small M by a launch of its
+  // own before the block
+  const bool side = q && q_side(M);
   int64_t block = 0;  // v-block major, m-block minor
   for (int64_t v0 = 0, vblock = 0; v0 < V; v0 += B.Vc, ++vblock) {
     const int64_t vc = std::min(B.Vc, V - v0);
-    if (q) {
-      if (launch_dequant(q->wq, q->scales, q->biases, q->bits, q->group, v0, vc, d, V, Wb, status, st) != cudaSuccess ||
-          !encode_w(Wb, vc))
-        return ORPO_ERR_CUDA;
-    }
+    if (q && (vblock == 0 || !side) &&
+        launch_dequant(q->wq, q->scales, q->biases, q->bits, q->group, v0, vc, d, V, qbuf_ptr(workspace, ql, vblock),
+                       status, st) != cudaSuccess)
+      return ORPO_ERR_CUDA;
+    if (q && !encode_w(qbuf_ptr(workspace, ql, vblock), vc)) return ORPO_ERR_CUDA;
     for (int64_t m0 = 0; m0 < M; m0 += B.Mc) {
       const int64_t mc = std::min(B.Mc, M - m0);
       const int n_mt = (int)cdiv(mc, kBM);
@@ -472,6 +504,10 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
         R.eps = eps;
       }
       ++block;
+      const int64_t n0 = v0 + B.Vc;
+      R.side = side && m0 == 0 && n0 < V ? dequant_job(q->wq, q->scales, q->biases, q->bits, q->group, n0,
+                                                    std::min(B.Vc, V - n0), d, V, qbuf_ptr(workspace, ql, vblock + 1))
+                                      : DequantJob{};
       if (launch_recompute(R, st) != cudaSuccess) return ORPO_ERR_CUDA;
 
       const GemmClassH cdw =
@@ -506,8 +542,7 @@ size_t orpo_head_workspace_bytes(int64_t M, int64_t V, int64_t d) {
 
 size_t orpo_head_q_workspace_bytes(int64_t M, int64_t V, int64_t d) {
   if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return 0;
-  return std::max(partial_bytes(M, kNsplitMaxQ), scratch_bytes(M, V) + kCounterBytes + kSkipBytes) +
-         wblock_bytes(M, V, d) + 2048;
+  return q_layout(M, V, d).total;
 }
 
 int orpo_head_fwd(const void* h, const void* W, const int32_t* targets, const uint8_t* mask, int64_t M, int64_t V,

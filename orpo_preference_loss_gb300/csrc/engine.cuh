@@ -4,7 +4,8 @@
 // One CTA per SM.  Warp 0 issues TMA loads into a shared-memory ring of stages,
 // warp 1 issues tcgen05.mma (one thread) into a double-buffered TMEM accumulator
 // (2 x 256 fp32 columns = all 512 columns), warps 2..5 run the epilogue that the
-// kernel supplies.  Each CTA's accumulator tile is BM x BN = 128 x 256, built from
+// kernel supplies, and warps 6..8 run an optional side job of the kernel's (the
+// quantised head dequantises its next vocabulary block there) or leave at once.  Each CTA's accumulator tile is BM x BN = 128 x 256, built from
 // BK = 64 wide k-blocks (128-byte swizzle rows) of bf16 operands.
 //
 // Two forms, chosen by the template argument CG (the tcgen05 CTA group):
@@ -44,7 +45,10 @@ constexpr int BK = 64;
 constexpr int MAX_STAGES = 6;
 constexpr int UMMA_K = 16;
 constexpr int EPI_WARPS = 4;
-constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int SIDE_WARP = 2 + EPI_WARPS;  // the first spare warp
+constexpr int SIDE_WARPS = 3;             // one spare warp took ~0.7 ms to dequantise an e4b block; three take
+                                          // about as long as the block's contraction
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS + 32 * SIDE_WARPS;
 constexpr int TMEM_COLS = 512;
 
 constexpr uint32_t A_BYTES = BM * BK * 2;            // 16 KiB
@@ -463,12 +467,14 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t box, int lane, const uin
 
 // ---------------------------------------------------------------- CTA driver
 
-// Runs the three roles; `epilogue(staging, ctl, tmem_base, warp, lane, rank)` is the kernel's
-// epilogue loop (`staging` is the base of the epilogue warps' staging boxes, STAGING_PER_WARP bytes
-// per warp), which walks the units with feed_consume<CG>(feed, ctl, i, status, true, rank).
+// Runs the roles; `epilogue(staging, ctl, tmem_base, warp, lane, rank)` is the kernel's epilogue loop
+// (`staging` is the base of the epilogue warps' staging boxes, STAGING_PER_WARP bytes per warp),
+// which walks the units with feed_consume<CG>(feed, ctl, i, status, true, rank); `side()` is the
+// spare warps' job, independent of the pipeline (it touches no barrier, TMEM or staging box).
 // CG = 2 must run in 2-CTA clusters.
-template <int CG, class Sched, class EpiFn>
-__device__ __forceinline__ void run_cta(const Sched& sched, const Feed& feed, int32_t* status, EpiFn&& epilogue) {
+template <int CG, class Sched, class EpiFn, class SideFn>
+__device__ __forceinline__ void run_cta(const Sched& sched, const Feed& feed, int32_t* status, EpiFn&& epilogue,
+                                        SideFn&& side) {
   using G = Geo<CG>;
   uint8_t* smem = smem_base_aligned();
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + G::CTL_OFF);
@@ -506,8 +512,10 @@ __device__ __forceinline__ void run_cta(const Sched& sched, const Feed& feed, in
     if (lane == 0) producer_role<CG>(sched, feed, smem, ctl, status, rank);
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) mma_role<CG>(sched, feed, smem, ctl, tmem_base, status);
-  } else {
+  } else if (warp < SIDE_WARP) {
     epilogue(smem + G::STAGING_OFF, ctl, tmem_base, warp, lane, rank);
+  } else {
+    side();
   }
   __syncwarp();
   tc_fence_before();

@@ -72,6 +72,7 @@ struct RecArgs {
   uint32_t* rowbits;   // filter instances: kept tiles by row tile, [n_mt][ld_row] bitmap over vt
   uint32_t* colbits;   //                   and by vocabulary tile, [n_vt][ld_col] bitmap over mt
   int ld_row, ld_col;
+  DequantJob side;     // spare warps: dequantise the next vocabulary block (quantised head), or nothing
 };
 
 // dZ for 32 accumulator values of one row starting at vocabulary column col0;
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
-  });
+  }, [&] { side_dequant(p.side, p.status); });
 }
 
 // ================================================================ fp32-output GEMM (dh, dW, diagnostic)
@@ -436,7 +437,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
-  });
+  }, [] {});
 }
 
 }  // namespace
@@ -450,7 +451,7 @@ cudaError_t launch_rec_kernel(const RecLaunch& L, cudaStream_t st) {
   const int chunk = L.chunk > 0 && L.chunk < n_mu ? L.chunk : n_mu;
   RecSched<CG> sched{nullptr, nullptr, L.m0, L.v0, L.n_mt, L.n_vt, L.kblocks, L.w_row0, L.list, L.count, chunk};
   RecArgs a{L.targets, L.mask, L.lse, L.g, L.M, L.V, L.softcap, L.status, L.eps, L.rowbits, L.colbits, L.ld_row,
-            L.ld_col};
+            L.ld_col, L.side};
   prof_begin(K_REC, st);
   const cudaError_t e =
       launch_engine(rec_kernel<cap, kFilter, CG>, CG, L.grid, Geo<CG>::SMEM, st, L.mh, L.mw, L.ms_store, sched, a);

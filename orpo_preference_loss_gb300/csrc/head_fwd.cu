@@ -77,6 +77,7 @@ struct FwdArgs {
                  // rows and one 256-column vocabulary tile (-inf for a group with no such row)
   int bmax_ld;   // ceil(V / 256)
   int part_cap;  // splits the partial arrays hold (each Mpad floats)
+  DequantJob side;  // spare warps: dequantise the next vocabulary block (quantised head), or nothing
 };
 
 // Per-row online softmax state of one epilogue thread, base-2 units.
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         p.part_s[(size_t)(p.split0 + s) * p.Mpad + row] = st.s;
       }
     }
-  });
+  }, [&] { side_dequant(p.side, p.status); });
 }
 
 // lse[t] = ln2 * (gM + log2 sum_k s_k 2^(m_k - gM));  logp[t] = z~[t,y_t] - lse[t] on response rows.
@@ -260,8 +261,8 @@ cudaError_t launch_fwd_kernel(const FwdLaunch& L, cudaStream_t st) {
   const int n_mu = (L.n_mt + CG - 1) / CG;
   const int chunk = L.chunk > 0 && L.chunk < n_mu ? L.chunk : n_mu;
   FwdSched<CG> sched{nullptr, nullptr, L.n_mt, L.nsplit, L.n_vt, L.kblocks, chunk, 0};
-  FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M,      L.Mpad,
-            L.V,       L.softcap, L.status, L.col0, L.split0, L.bmax, (L.V + BN - 1) / BN, L.part_cap};
+  FwdArgs a{L.targets, L.mask, L.logp, L.part_m, L.part_s, L.M,      L.Mpad,       L.V,
+            L.softcap, L.status, L.col0, L.split0, L.bmax, (L.V + BN - 1) / BN, L.part_cap, L.side};
   prof_begin(K_FWD, st);
   const cudaError_t e = launch_engine(fwd_kernel<cap, CG>, CG, L.grid, Geo<CG>::SMEM, st, L.mh, L.mw, sched, a);
   prof_end(K_FWD, st);

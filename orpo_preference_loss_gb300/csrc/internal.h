@@ -7,6 +7,8 @@
 
 #include <atomic>
 
+#include "quant.cuh"
+
 namespace orpo {
 
 // ---- kernels using more than 48 KiB of dynamic shared memory opt in once per device
@@ -74,6 +76,7 @@ struct FwdLaunch {
   float* bmax = nullptr;  // optional block maxima [ceil(M/32), ceil(V/256)] (base-2 softcapped logits)
   int chunk = 0;          // M units (row tiles, or pairs of them) per L2 chunk (l2_chunk); 0: all of them
   int cg = 1;             // CTA group; grid = cg x (CTAs or clusters)
+  DequantJob side{};      // quantised head: the next block's dequantisation, done by the spare warps
 };
 cudaError_t launch_forward(const FwdLaunch& L, cudaStream_t st);  // logits kernel + merge of L.nsplit splits
 cudaError_t launch_forward_logits(const FwdLaunch& L, cudaStream_t st);
@@ -101,6 +104,7 @@ struct RecLaunch {
   float eps = 0.f;
   int chunk = 0;                // M units per L2 chunk (l2_chunk); 0: all of them
   int cg = 1;                   // CTA group (1 whenever the skip bitmaps or lists are used)
+  DequantJob side{};            // quantised head: the next block's dequantisation, done by the spare warps
 };
 cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st);
 
@@ -142,6 +146,8 @@ cudaError_t launch_skip_plan(const SkipPlan& P, cudaStream_t st);  // lists and 
 cudaError_t launch_dequant(const uint8_t* wq, const void* scales, const void* biases, int bits, int group,
                            int64_t v0, int64_t rows, int64_t d, int64_t V, void* out_bf16, int32_t* status,
                            cudaStream_t st);
+DequantJob dequant_job(const uint8_t* wq, const void* scales, const void* biases, int bits, int group, int64_t v0,
+                       int64_t rows, int64_t d, int64_t V, void* out_bf16);
 
 // ---- generic two-class GEMM with an fp32 store / reduce-add epilogue
 struct GemmClassH {

@@ -8,7 +8,7 @@ import torch
 import oracle
 import orpo_preference_loss_gb300 as orpo
 import workloads
-from gpu_helpers import GRAD_RELFRO, LOGP_ATOL, dev, f64, gpu_backward, relfro, status_tensor, to_dev
+from gpu_helpers import GRAD_RELFRO, LOGP_ATOL, dev, f64, gpu_backward, gpu_forward, relfro, status_tensor, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -66,6 +66,30 @@ def test_quantised_backward_is_the_bf16_backward_on_the_dequantised_weights():
     # frozen head: dW skipped, dh unchanged
     out2, st3 = run_q(t, q, 4, 64, w, 0.0, g=res.g, lse_in=lse_r, with_dw=False)
     assert st3 == 0 and out2["dW"] is None and np.array_equal(out2["dh"], dh)
+
+
+def test_blocks_dequantised_by_the_spare_warps_are_the_bf16_path_bit_for_bit():
+    """At M >= 8192 every vocabulary block after the first is dequantised by the spare warps of the
+    previous block's kernels while it is multiplied; the backward must still equal the bf16 backward
+    fed the dequantised weights bit for bit (same blocks, same tiles), the forward the oracle."""
+    w = workloads.make("small", M=8200, d=256, V=70000)
+    assert w.M >= 8192
+    q, Wd = quant_dev(w, 4, 64)
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([[0, w.M - 1], rng.choice(w.M, 40, replace=False)]))
+    logp_r, lse_r = oracle.head_forward(f64(w.h[rows]), Wd, w.targets[rows], w.mask[rows], 0.0)
+    g = (rng.standard_normal(w.M) * 1e-3).astype(np.float32)
+    w2 = workloads.make("small", M=8200, d=256, V=70000)
+    w2.W = workloads.round_bf16(Wd.astype(np.float32))          # exact: Wd already holds bf16 values
+    t2 = to_dev(w2)
+    _, lse_in, st0 = gpu_forward(t2, w.M, w.V, w.d, 0.0)          # any lse serves a bitwise comparison
+    t = to_dev(w)
+    out, st = run_q(t, q, 4, 64, w, 0.0, g=g, lse_in=lse_in)
+    assert st0 == 0 and st == 0
+    assert np.max(np.abs(out["logp"][rows] - logp_r)) < LOGP_ATOL and np.max(np.abs(out["lse"][rows] - lse_r)) < LOGP_ATOL
+    dh, dW, st2 = gpu_backward(t2, lse_in, g, w.M, w.V, w.d, 0.0)
+    assert st2 == 0
+    assert np.array_equal(out["dh"], dh) and np.array_equal(out["dW"], dW)
 
 
 def test_quantised_e4b_full_size_several_blocks():
