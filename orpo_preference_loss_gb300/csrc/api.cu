@@ -130,6 +130,53 @@ constexpr size_t kCounterBytes = kCounters * sizeof(int);
 // 120 or more blocks.
 constexpr size_t kSkipBytes = 4 << 20;
 
+// Split K of the dh GEMM.  With few rows the dh class has few output tiles, each with K = the block's
+// vocabulary columns (at M 512, d 2560: 20 units of 4096 k-blocks on 76 clusters), so most SMs idle.
+// Each tile's K range is then cut into parts (see split_part in head_bwd.cu); the area after the skip
+// area holds the parts' fp32 tiles and one counter per tile.
+constexpr int kSplitSlotsMax = 320;  // partial tiles (128 x 256 fp32, 128 KiB each) the area holds
+constexpr int kSplitMax = 8;         // parts per tile (the kernel's kSplitMaxParts)
+constexpr int kSplitMinKb = 8;       // k-blocks per part at least
+constexpr int kSplitFinalKb = 96;    // the last part's read-and-sum of every part, in k-block times
+constexpr int64_t kSlotBytes = (int64_t)kBM * kBN * 4;
+
+int64_t dh_tiles(int64_t M, int64_t d, int64_t qd = 0) {  // CTA tiles of the dh class of a full row block
+  return cdiv(bwd_blocks(M, 1, qd).Mc, kBM) * cdiv(d, kBN);
+}
+
+size_t split_part_bytes(int64_t M, int64_t d, int64_t qd = 0) {
+  const int64_t t = dh_tiles(M, d, qd);
+  if (t > kSplitSlotsMax / 2) return 0;  // not even two parts fit: never split
+  return (size_t)std::min<int64_t>(kSplitSlotsMax, t * kSplitMax) * kSlotBytes;
+}
+
+size_t split_bytes(int64_t M, int64_t d, int64_t qd = 0) {
+  const size_t pb = split_part_bytes(M, d, qd);
+  return pb ? pb + (((size_t)dh_tiles(M, d, qd) * 4 + 1023) & ~size_t(1023)) : 0;
+}
+
+// Parts per dh tile.  The launch takes at least (all its k-blocks) / slots, the dh units' own waves
+// (waves of parts) x (k-blocks per part + 2 for writing the partial tile) + the last part's sum of all
+// parts (a fixed cost: its loads are all in flight at once).  Minimise the larger of the two; ties
+// to fewer parts.  A short K (the tiny config's 64 k-blocks) is not split, nor a launch whose other
+// class (`other_kb` k-blocks of dW units) already fills the slots.
+int choose_ksplit(int64_t units, int64_t kblocks, int64_t tiles, int slots, size_t part_bytes, int64_t other_kb) {
+  if (part_bytes == 0) return 1;
+  const int64_t smax = std::min<int64_t>({(int64_t)kSplitMax, (int64_t)(part_bytes / kSlotBytes) / tiles,
+                                          kblocks / kSplitMinKb});
+  const int64_t floor_kb = cdiv(units * kblocks + other_kb, slots);
+  int best = 1;
+  int64_t best_cost = std::max(floor_kb, cdiv(units, slots) * kblocks);
+  for (int64_t k = 2; k <= smax; ++k) {
+    const int64_t cost = std::max(floor_kb, cdiv(units * k, slots) * (cdiv(kblocks, k) + 2) + kSplitFinalKb);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = (int)k;
+    }
+  }
+  return best;
+}
+
 SkipShape skip_shape(const BwdBlocks& b) {
   SkipShape s{};
   s.n_mt = (int)(b.Mc / kBM);
@@ -244,7 +291,8 @@ QLayout q_layout(int64_t M, int64_t V, int64_t d) {
   L.rows = bwd_blocks(M, V, d).Vc;
   L.nblocks = cdiv(V, L.rows);
   L.nsplit_cap = (int)std::max<int64_t>(kNsplitMaxQ, L.nblocks);
-  const size_t head = std::max(partial_bytes(M, L.nsplit_cap), scratch_bytes(M, V, d) + kCounterBytes + kSkipBytes);
+  const size_t head =
+      std::max(partial_bytes(M, L.nsplit_cap), scratch_bytes(M, V, d) + kCounterBytes + kSkipBytes + split_bytes(M, d, d));
   const size_t buf = ((size_t)L.rows * d * 2 + 1023) & ~size_t(1023);
   L.buf_off[0] = (head + 1023) & ~size_t(1023);
   L.buf_off[1] = L.buf_off[0] + (q_side(M) ? buf : 0);
@@ -421,6 +469,11 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   }
   const QLayout ql = q ? q_layout(M, V, d) : QLayout{};
   int64_t launch = 0;
+  // split-K area after the skip area: partial tiles, then one counter per dh tile (zeroed once per call)
+  const size_t split_parts = skip ? 0 : split_part_bytes(M, d, q ? d : 0);
+  float* split_part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(counters + kCounters) + kSkipBytes);
+  int* split_cnt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(split_part) + split_parts);
+  bool split_zeroed = false;
   const int64_t sp = scratch_pitch(B);
   // the skips' bitmaps and tile lists are per 128-row tile
   const Placement pr = placement(sms, false, !skip);  // recompute
@@ -512,17 +565,26 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
 
       const GemmClassH cdw =
           dW ? dw_class(v0, vc, m0, mc, V, d, accumulate_dW, skip ? colbits : nullptr, P.shape.ld_col) : GemmClassH{};
-      const GemmClassH cdh =
-          dh_class(vc, m0, mc, M, d, vblock > 0, q ? 0 : v0, skip ? rowbits : nullptr, P.shape.ld_row);
-      // longer tiles first
-      if (dW && cdw.kblocks >= cdh.kblocks) {
+      GemmClassH cdh = dh_class(vc, m0, mc, M, d, vblock > 0, q ? 0 : v0, skip ? rowbits : nullptr, P.shape.ld_row);
+      const int64_t dw_kb = dW ? cdiv(cdw.n_mt, pl.cg) * cdw.n_nt * cdw.kblocks : 0;
+      cdh.ksplit = choose_ksplit(cdiv(cdh.n_mt, pl.cg) * cdh.n_nt, cdh.kblocks, (int64_t)cdh.n_mt * cdh.n_nt, pl.slots,
+                                 split_parts, dw_kb);
+      if (cdh.ksplit > 1) {
+        cdh.part = split_part;
+        cdh.cnt = split_cnt;
+        if (!split_zeroed && cudaMemsetAsync(split_cnt, 0, (size_t)dh_tiles(M, d, q ? d : 0) * 4, st) != cudaSuccess)
+          return ORPO_ERR_CUDA;
+        split_zeroed = true;
+      }
+      // longer units first
+      if (dW && cdw.kblocks >= cdiv(cdh.kblocks, cdh.ksplit)) {
         G.cls[0] = cdw;
         G.cls[1] = cdh;
       } else {
         G.cls[0] = cdh;
         G.cls[1] = cdw;
       }
-      const int64_t units = cdiv(cdw.n_mt, pl.cg) * cdw.n_nt + cdiv(cdh.n_mt, pl.cg) * cdh.n_nt;
+      const int64_t units = cdiv(cdw.n_mt, pl.cg) * cdw.n_nt + cdiv(cdh.n_mt, pl.cg) * cdh.n_nt * cdh.ksplit;
       G.grid = (int)std::min<int64_t>(units, pl.slots) * pl.cg;
       if (launch % kCounters == 0 && cudaMemsetAsync(counters, 0, kCounterBytes, st) != cudaSuccess)
         return ORPO_ERR_CUDA;
@@ -537,7 +599,8 @@ extern "C" {
 
 size_t orpo_head_workspace_bytes(int64_t M, int64_t V, int64_t d) {
   if (M < 0 || M > kMaxRows || V < 1 || V > kMaxRows || d < 8 || d >= (1 << 20)) return 0;
-  return std::max(partial_bytes(M, kNsplitMax), scratch_bytes(M, V) + kCounterBytes + kSkipBytes) + 1024;
+  return std::max(partial_bytes(M, kNsplitMax), scratch_bytes(M, V) + kCounterBytes + kSkipBytes + split_bytes(M, d)) +
+         1024;
 }
 
 size_t orpo_head_q_workspace_bytes(int64_t M, int64_t V, int64_t d) {

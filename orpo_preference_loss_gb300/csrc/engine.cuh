@@ -87,6 +87,7 @@ struct SmemCtl {
   volatile int unit_ring[RING];
   uint32_t tmem_base;
   volatile int abort_flag;
+  volatile int split_last;  // split-K epilogue: this CTA counted a tile's last part
 };
 static_assert(sizeof(SmemCtl) <= SMEM_CTL_BYTES, "control block too large");
 

@@ -264,6 +264,12 @@ struct GemmClass {
   const uint32_t* kbits;
   int kwords, list_shift, kg_shift, ngroups, clip;
   int kbits_rows;  // bitmaps at kbits
+  // split K (dense classes only): each output tile's K range in ksplit parts, each part a unit that
+  // writes its fp32 partial tile to part[tile][part]; the tile's last part to finish (counted in
+  // cnt[tile], which it resets to 0) sums the parts in part order and writes the tile.
+  int ksplit;
+  float* part;
+  int* cnt;
 };
 
 // Unit = (class, M unit, N tile); an M unit is one 128-row output tile (CG = 1) or a pair's two
@@ -295,14 +301,17 @@ struct GemmSched {
     return c;
   }
   __device__ static int n_mu(const GemmClass& c) { return (c.n_mt + CG - 1) / CG; }
-  __device__ int n0() const { return n_mu(cls[0]) * cls[0].n_nt; }
-  __device__ int num_units() const { return n0() + n_mu(cls[1]) * cls[1].n_nt; }
+  __device__ int n0() const { return n_mu(cls[0]) * cls[0].n_nt * cls[0].ksplit; }
+  __device__ int num_units() const { return n0() + n_mu(cls[1]) * cls[1].n_nt * cls[1].ksplit; }
   __device__ int unit_len(int) const { return 1; }
-  // mt: this CTA's output row tile (c.n_mt or more: the empty half of a pair whose tile count is odd)
-  __device__ void decode(int u, int& k, int& mt, int& nt) const {
+  // mt: this CTA's output row tile (c.n_mt or more: the empty half of a pair whose tile count is odd);
+  // ks: the part of the tile's K range (0 without split K).  The parts of a tile are consecutive units.
+  __device__ void decode(int u, int& k, int& mt, int& nt, int& ks) const {
     k = u < n0() ? 0 : 1;
-    const int v = k == 0 ? u : u - n0();
     const GemmClass c = pick(k);
+    const int w = k == 0 ? u : u - n0();
+    const int v = w / c.ksplit;
+    ks = w - v * c.ksplit;
     int mu;
     if (c.mt_major) {
       mu = v / c.n_nt;
@@ -313,14 +322,19 @@ struct GemmSched {
     }
     mt = mu * CG + rank;
   }
+  // k-blocks [kb_first(c, ks), kb_first(c, ks + 1)) form part ks
+  __device__ static int kb_first(const GemmClass& c, int ks) {
+    return (int)(((long long)ks * c.kblocks) / c.ksplit);
+  }
   __device__ TileOps tile(int u, int) const {
-    int k, mt, nt;
-    decode(u, k, mt, nt);
+    int k, mt, nt, ks;
+    decode(u, k, mt, nt, ks);
     const GemmClass c = pick(k);
+    const int kb0 = kb_first(c, ks);
     TileOps t;
-    t.a = Operand{map(c.a_map), c.a_mn, c.a_mn_base + mt * BM, c.a_k_base};
-    t.b = Operand{map(c.b_map), c.b_mn, c.b_mn_base + nt * BN + rank * (BN / CG), c.b_k_base};
-    t.kblocks = c.kblocks;
+    t.a = Operand{map(c.a_map), c.a_mn, c.a_mn_base + mt * BM, c.a_k_base + kb0 * BK};
+    t.b = Operand{map(c.b_map), c.b_mn, c.b_mn_base + nt * BN + rank * (BN / CG), c.b_k_base + kb0 * BK};
+    t.kblocks = kb_first(c, ks + 1) - kb0;
     if (CG == 1 && c.kbits != nullptr) {
       const int br = in_bounds(status, mt >> c.list_shift, c.kbits_rows) ? mt >> c.list_shift : 0;
       const uint32_t* bits = c.kbits + (size_t)br * c.kwords;
@@ -336,6 +350,107 @@ struct GemmSched {
     return t;
   }
 };
+
+__device__ __forceinline__ void epi_bar_sync() {  // the four epilogue warps of this CTA
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
+}
+
+// One part of a split-K tile (`c.ksplit` > 1), run by the four epilogue warps: this CTA's fp32
+// accumulator goes to the part's slot (float4 index (col / 4) * BM + row: a warp's stores of one
+// column group are contiguous); after a fence, one thread counts the part in.  The part counted last
+// (whichever CTA runs it) reads every part's slot in part order (ld.global.cg: from L2, written by
+// other SMs), adds them in that order, writes the tile as the unsplit epilogue would (store or
+// reduce-add) and resets the counter for the next launch.  No CTA waits for another, and the sum
+// is the same whichever part is last, so results stay bitwise reproducible.
+constexpr int kSplitMaxParts = 8;  // parts per tile at most (the host's kSplitMax)
+
+template <int CG>
+__device__ __forceinline__ void split_part(const GemmClass& c, SmemCtl* ctl, uint32_t taddr, int mt, int nt, int ks,
+                                           int q, int warp, int lane, int orow, int ocol0, const CUtensorMap* out,
+                                           uint32_t staging, uint8_t* stage_ptr, uint32_t& nstore, uint32_t tcount,
+                                           uint32_t rank, int32_t* status) {
+  constexpr int kSlot = BM * BN / 4;  // float4 per partial tile
+  if (mt >= c.n_mt) {                 // the empty half of an odd pair: no tile, no count
+    epi_release<CG>(ctl, tcount, rank);
+    return;
+  }
+  const int tile = mt * c.n_nt + nt;
+  if (!in_bounds(status, tile, (int64_t)c.n_mt * c.n_nt) || !in_bounds(status, ks, c.ksplit)) {
+    epi_release<CG>(ctl, tcount, rank);
+    return;
+  }
+  const int r = 32 * q + lane;  // this thread's row of the tile
+  float4* slots = reinterpret_cast<float4*>(c.part) + (size_t)tile * c.ksplit * kSlot;
+  float4* mine = slots + (size_t)ks * kSlot;
+  uint32_t v[32];
+#pragma unroll 1
+  for (int ch = 0; ch < BN / 32; ++ch) {
+    tmem_ld32(taddr + ch * 32, v);
+    tmem_ld_wait(v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      mine[(ch * 8 + j) * BM + r] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+  }
+  epi_release<CG>(ctl, tcount, rank);
+  __threadfence();
+  epi_bar_sync();
+  if (warp == 2 && lane == 0) ctl->split_last = atomicAdd(c.cnt + tile, 1) == c.ksplit - 1 ? 1 : 0;
+  epi_bar_sync();
+  if (!ctl->split_last) return;
+  __threadfence();
+  if (orow < c.out_rows) {
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+      const int col = ocol0 + ch * 32;
+      if (col >= c.out_cols) break;
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {  // two float4 columns at a time: every part's loads in flight at once
+        float4 x[2][kSplitMaxParts];
+#pragma unroll
+        for (int p = 0; p < kSplitMaxParts; ++p) {
+          if (p < c.ksplit) {
+            x[0][p] = __ldcg(slots + (size_t)p * kSlot + (ch * 8 + j) * BM + r);
+            x[1][p] = __ldcg(slots + (size_t)p * kSlot + (ch * 8 + j + 1) * BM + r);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float4 acc = x[e][0];
+#pragma unroll
+          for (int p = 1; p < kSplitMaxParts; ++p) {
+            if (p < c.ksplit) {  // in part order
+              acc.x += x[e][p].x;
+              acc.y += x[e][p].y;
+              acc.z += x[e][p].z;
+              acc.w += x[e][p].w;
+            }
+          }
+          v[4 * (j + e)] = __float_as_uint(acc.x);
+          v[4 * (j + e) + 1] = __float_as_uint(acc.y);
+          v[4 * (j + e) + 2] = __float_as_uint(acc.z);
+          v[4 * (j + e) + 3] = __float_as_uint(acc.w);
+        }
+      }
+      const uint32_t box = staging + (nstore & 1u) * BOX_BYTES;
+      if (lane == 0) bulk_wait_group_read<1>();
+      __syncwarp();
+      stage_row_f32(box, lane, v);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const void* src = stage_ptr + (nstore & 1u) * BOX_BYTES;
+        if (c.reduce)
+          tma_reduce_add_2d(out, src, col, orow);
+        else
+          tma_store_2d(out, src, col, orow);
+        bulk_commit_group();
+      }
+      ++nstore;
+    }
+  }
+  if (warp == 2 && lane == 0) c.cnt[tile] = 0;
+}
 
 template <int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -364,8 +479,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (uint32_t i = 0;; ++i) {
       const int u = feed_consume<CG>(feed, ctl, i, status, true, rank);
       if (u < 0) break;
-      int k, mt, nt;
-      sched.decode(u, k, mt, nt);
+      int k, mt, nt, ks;
+      sched.decode(u, k, mt, nt, ks);
       const GemmClass c = sched.pick(k);
       const CUtensorMap* out = sched.map(c.out_map);
       const int orow = c.out_row_base + mt * BM + 32 * q;
@@ -395,6 +510,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       uint32_t taddr;
       if (!epi_acquire<CG>(ctl, tmem_base, tcount, warp, status, &taddr)) break;
+      if (c.ksplit > 1) {
+        split_part<CG>(c, ctl, taddr, mt, nt, ks, q, warp, lane, orow, ocol0, out, staging, stage_ptr, nstore, tcount,
+                       rank, status);
+        ++tcount;
+        continue;
+      }
       if (mt < c.n_mt && orow < c.out_rows) {  // (the empty half of an odd pair stores nothing)
         uint32_t ra[32], rb[32];
         tmem_ld32(taddr, ra);
@@ -480,7 +601,7 @@ cudaError_t launch_gemm_cg(const GemmLaunch& L, cudaStream_t st, int kind) {
                              h.b_mn_base, h.b_k_base,  h.out_map,    h.out_row_base, h.out_col_base, h.reduce,
                              h.out_rows,  h.out_cols,  h.n_mt,       h.n_nt,         h.kblocks,      h.mt_major,
                              h.kbits,     h.kwords,    h.list_shift, h.kg_shift,     h.ngroups,      h.clip,
-                             h.kbits_rows};
+                             h.kbits_rows, h.ksplit,   h.part,       h.cnt};
   }
   prof_begin(kind, st);
   const cudaError_t e = launch_engine(gemm_kernel<CG>, CG, L.grid, Geo<CG>::SMEM, st, L.maps[0], L.maps[1], L.maps[2],

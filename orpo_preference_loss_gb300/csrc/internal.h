@@ -162,6 +162,11 @@ struct GemmClassH {
   const uint32_t* kbits = nullptr;
   int kwords = 0, list_shift = 0, kg_shift = 0, ngroups = 0, clip = 0;
   int kbits_rows = 0;  // bitmaps at kbits (bounds-checked build)
+  // split K (dense only): K in ksplit parts; part holds n_mt * n_nt * ksplit fp32 tiles of 128 x 256,
+  // cnt n_mt * n_nt zeroed counters (reset by the kernel after use)
+  int ksplit = 1;
+  float* part = nullptr;
+  int* cnt = nullptr;
 };
 struct GemmLaunch {
   CUtensorMap maps[6];   // B operands' boxes cover kBN / cg rows or columns
