@@ -490,7 +490,10 @@ def ours(args, w, rank, world, local):
                            backward=(f"skips at eps {args.skip_eps:g} (coefficient filter + block skip); "
                                      "tflops counts the dense 6MVd" if skip else "exact"),
                            parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
-            "tflops": tflops, "frac_of_peak": tflops / burst, "frac_of_sustained_peak": tflops / sustained,
+            "tflops": tflops,
+            # with the backward skips, tflops counts the dense work the skips avoid: no fraction of peak
+            "frac_of_peak": None if skip else tflops / burst,
+            "frac_of_sustained_peak": None if skip else tflops / sustained,
             "peak_extra_gb": peak_extra / 1e9, "e2e": e2e, "gpu_launches": sum(v["launches"] for v in
                                                                                kernels.values()),
             "kernels": kernels, "roofline": roof, "clocks": clk}

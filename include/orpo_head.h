@@ -81,8 +81,11 @@ enum {
  * Bytes of scratch that orpo_head_fwd and orpo_head_bwd need for these sizes
  * (one workspace serves both).  It holds the per-vocab-split partials of the
  * forward (O(M)) and the bounded bf16 block of logit gradients that the
- * backward streams through (at most 256 MiB whatever M and V are), so the
- * extra memory never grows like M * V.  Returns 0 for invalid sizes.
+ * backward streams through (at most 256 MiB whatever M and V are), and, for
+ * batches whose dh GEMM has few output tiles (at most 160 tiles of 128 x 256,
+ * e.g. M <= 2048 at d = 2560), up to 40 MiB of fp32 partial tiles with which
+ * that GEMM splits its K range over more SMs.  The extra memory never grows
+ * like M * V.  Returns 0 for invalid sizes.
  */
 size_t orpo_head_workspace_bytes(int64_t M, int64_t V, int64_t d);
 
