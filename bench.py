@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the step")
     ap.add_argument("--clocks-csv", default=None,
                     help="keep the raw nvidia-smi clock samples of the timed region in this file")
     ap.add_argument("--loss", default="orpo", choices=["orpo", "simpo", "dpo", "ipo", "hinge", "orpo_full"],
@@ -385,6 +386,36 @@ def ours(args, w, rank, world, local):
     ms_step = ms / args.steps
     value = world * M * args.steps / (ms / 1e3)
 
+    # ---- the same step replayed from a CUDA graph (OrpoHead.capture does this for a caller): one
+    # launch per step instead of 5-35, which matters for the launch-bound small shapes.  Reported
+    # beside the eager value, which stays the headline (its per-kernel launch timing needs eager
+    # launches).
+    graph_line = None
+    if not args.no_graph:
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            step()
+        for _ in range(args.warmup):
+            cg.replay()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for _ in range(args.steps):
+            cg.replay()
+        r1.record(stream)
+        torch.cuda.synchronize()
+        gms = r0.elapsed_time(r1)
+        if world > 1:
+            x = torch.tensor([gms], device=dev)
+            dist.all_reduce(x, op=dist.ReduceOp.MAX)
+            gms = float(x.item())
+        graph_line = {"value": world * M * args.steps / (gms / 1e3), "unit": "tokens/s",
+                      "ms_per_step": gms / args.steps,
+                      "how": "the whole step captured once in a CUDA graph and replayed K times, device-timed"}
+        del cg
+
     # ---- end to end through host buffers: every step copies its inputs from pinned host memory
     # and reads its loss / metrics back.  Two device input sets and a copy stream let the copy of
     # step k + 1's inputs run while step k computes; step k waits for its own copy.
@@ -494,8 +525,8 @@ def ours(args, w, rank, world, local):
             # with the backward skips, tflops counts the dense work the skips avoid: no fraction of peak
             "frac_of_peak": None if skip else tflops / burst,
             "frac_of_sustained_peak": None if skip else tflops / sustained,
-            "peak_extra_gb": peak_extra / 1e9, "e2e": e2e, "gpu_launches": sum(v["launches"] for v in
-                                                                               kernels.values()),
+            "peak_extra_gb": peak_extra / 1e9, "e2e": e2e, "graph": graph_line,
+            "gpu_launches": sum(v["launches"] for v in kernels.values()),
             "kernels": kernels, "roofline": roof, "clocks": clk}
     if world == 1 and not args.no_cpu_baseline:
         idx = oracle_sample(w, 256)

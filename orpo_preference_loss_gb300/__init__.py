@@ -447,3 +447,23 @@ class OrpoHead:
             orpo_head_bwd(h, W, targets, mask, self.lse, self.g, softcap, self.dh, self.dW, accumulate_dW,
                           self.workspace, self.status, stream)
         return self.out
+
+    def capture(self, h, W, targets, mask, seq_id, softcap, lam, accumulate_dW=False):
+        """Record one step on these tensors into a CUDA graph and return it.
+
+        Each ``graph.replay()`` reruns the whole step (forward, loss, backward: 5 or more launches)
+        on whatever the given tensors hold at that moment, for the price of one launch; this matters
+        for small batches, whose step is a few launches of microseconds.  The step runs once eagerly
+        first, on a side stream, so that the library's one-time device set-up happens outside the
+        capture.  Fill the same input tensors before each replay; the outputs land in this head's
+        buffers as with step()."""
+        args = (h, W, targets, mask, seq_id, softcap, lam, accumulate_dW)
+        side = torch.cuda.Stream(self.workspace.device)
+        side.wait_stream(torch.cuda.current_stream(self.workspace.device))
+        with torch.cuda.stream(side):
+            self.step(*args)
+        torch.cuda.current_stream(self.workspace.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.step(*args)
+        return graph

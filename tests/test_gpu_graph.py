@@ -46,3 +46,26 @@ def test_step_replays_in_a_cuda_graph(skip_eps):
         for a, b in zip(got, ref):
             assert np.array_equal(a, b)
     assert int(head.status.item()) == 0
+
+
+def test_capture_replays_new_inputs_of_the_tiny_config():
+    """OrpoHead.capture on the tiny config (a launch-bound step): a replay after new values are
+    copied into the captured input tensors equals an eager step on those values, bit for bit."""
+    w1 = workloads.make("tiny")
+    w2 = workloads.make("tiny", seed=1)
+    t1, t2 = to_dev(w1), to_dev(w2)
+    bufs = {k: v.clone() for k, v in t1.items()}
+    h, W = bufs["h"].view(torch.bfloat16), bufs["W"].view(torch.bfloat16)
+    head = orpo.OrpoHead(w1.M, w1.V, w1.d, w1.n_pairs)
+    graph = head.capture(h, W, bufs["targets"], bufs["mask"], bufs["seq_id"], w1.softcap, w1.lam)
+    eager = orpo.OrpoHead(w1.M, w1.V, w1.d, w1.n_pairs)
+    for t, w in ((t2, w2), (t1, w1)):
+        for k in bufs:
+            bufs[k].copy_(t[k])
+        graph.replay()
+        eager.step(t["h"].view(torch.bfloat16), t["W"].view(torch.bfloat16), t["targets"], t["mask"], t["seq_id"],
+                   w.softcap, w.lam)
+        torch.cuda.synchronize()
+        for a, b in zip(outputs(head), outputs(eager)):
+            assert np.array_equal(a, b)
+    assert int(head.status.item()) == 0 and int(eager.status.item()) == 0
