@@ -207,11 +207,14 @@ int orpo_head_bwd(const void* h_bf16, const void* W_bf16, const int32_t* targets
  *   bits    4 or 8;  group  a multiple of 8 that divides d.
  * The head's weight is W[v, j] = bf16(scales[v, j/group] * q[v, j] + biases[v, j/group])
  * (fp32 arithmetic, one nearest-even rounding).  Each call walks W in vocabulary
- * blocks, dequantised alternately into two bf16 buffers of the workspace (at most
- * 128 MiB each, unless a single 256-row block is larger): the first block by a
- * launch of its own, every later one by a spare warp of each tensor-core kernel
- * while the previous block is multiplied.  The bf16 tensor-core path runs on the
- * dequantised blocks; nothing grows like V * d beyond the quantised weights.  dW, when given, is the gradient with respect to
+ * blocks dequantised into bf16 buffers of the workspace.  From M = 8192 rows on
+ * there are two buffers of at most 128 MiB: the first block is dequantised by a
+ * launch of its own, every later one by spare warps of the tensor-core kernels
+ * while the previous block is multiplied.  Below 8192 rows (where a block's
+ * contraction is too short to hide that work) there is one buffer of at most
+ * 256 MiB and a dequantisation launch per block.  (A single 256-row block can
+ * exceed these sizes when d is very large.)  The bf16 tensor-core path runs on
+ * the dequantised blocks; nothing grows like V * d beyond the quantised weights.  dW, when given, is the gradient with respect to
  * the dequantised weight.  The workspace must hold orpo_head_q_workspace_bytes.
  * Host errors: ORPO_ERR_ARG for bits / group, ORPO_ERR_ALIGN for wq alignment.
  */
