@@ -92,6 +92,21 @@ def test_blocks_dequantised_by_the_spare_warps_are_the_bf16_path_bit_for_bit():
     assert np.array_equal(out["dh"], dh) and np.array_equal(out["dW"], dW)
 
 
+def test_quantised_head_with_split_dh_matches_oracle():
+    """M 512 (the pages' batch size), d 256: the dh GEMM splits each tile's K range (65536 columns)
+    over several SMs, here on the dequantised weights, with one dequantisation launch per block."""
+    w = workloads.make("e4b", M=512, d=256, V=65536)
+    q, Wd = quant_dev(w, 4, 64)
+    logp_r, lse_r, res, dh_r, dW_r = oracle.full_chain(f64(w.h), Wd, w.targets, w.mask, w.seq_id, w.n_pairs, w.lam,
+                                                       w.softcap)
+    out, st = run_q(to_dev(w), q, 4, 64, w, w.softcap, g=res.g, lse_in=lse_r)
+    assert st == 0
+    assert np.max(np.abs(out["logp"] - logp_r)) < LOGP_ATOL and np.max(np.abs(out["lse"] - lse_r)) < LOGP_ATOL
+    assert relfro(out["dh"], dh_r) < GRAD_RELFRO and relfro(out["dW"], dW_r) < GRAD_RELFRO
+    out2, st2 = run_q(to_dev(w), q, 4, 64, w, w.softcap, g=res.g, lse_in=lse_r, with_dw=False)
+    assert st2 == 0 and np.array_equal(out2["dh"], out["dh"])
+
+
 def test_quantised_e4b_full_size_several_blocks():
     w = workloads.make("e4b")
     q, Wd = quant_dev(w, 4, 64)
