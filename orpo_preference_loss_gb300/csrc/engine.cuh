@@ -5,8 +5,9 @@
 // warp 1 issues tcgen05.mma (one thread) into a double-buffered TMEM accumulator
 // (2 x 256 fp32 columns = all 512 columns), warps 2..5 run the epilogue that the
 // kernel supplies, and warps 6..8 run an optional side job of the kernel's (the
-// quantised head dequantises its next vocabulary block there) or leave at once.  Each CTA's accumulator tile is BM x BN = 128 x 256, built from
-// BK = 64 wide k-blocks (128-byte swizzle rows) of bf16 operands.
+// quantised head dequantises its next vocabulary block there) or leave at once.
+// Each CTA's accumulator tile is BM x BN = 128 x 256, built from BK = 64 wide
+// k-blocks (128-byte swizzle rows) of bf16 operands.
 //
 // Two forms, chosen by the template argument CG (the tcgen05 CTA group):
 //   CG = 1  one CTA per tile.  A stage holds A (128 x 64) and B (256 x 64): 48 KiB, 4 stages.
@@ -88,6 +89,8 @@ struct SmemCtl {
   uint32_t tmem_base;
   volatile int abort_flag;
   volatile int split_last;  // split-K epilogue: this CTA counted a tile's last part
+  uint64_t split_in;        // split-K epilogue: the epilogue warps' partial rows are written
+  uint64_t split_out;       //                   split_last is set
 };
 static_assert(sizeof(SmemCtl) <= SMEM_CTL_BYTES, "control block too large");
 
@@ -491,6 +494,8 @@ __device__ __forceinline__ void run_cta(const Sched& sched, const Feed& feed, in
       mbar_init(&ctl->acc_empty[b], CG * EPI_WARPS);  // pair: both CTAs' epilogue warps
     }
     mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->split_in, EPI_WARPS);
+    mbar_init(&ctl->split_out, 1);
     for (int r = 0; r < RING; ++r) {
       mbar_init(&ctl->unit_full[r], 1);
       // MMA thread + epilogue warps; pair: + the odd CTA's producer and epilogue warps

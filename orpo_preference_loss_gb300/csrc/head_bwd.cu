@@ -351,24 +351,22 @@ struct GemmSched {
   }
 };
 
-__device__ __forceinline__ void epi_bar_sync() {  // the four epilogue warps of this CTA
-  asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
-}
-
 // One part of a split-K tile (`c.ksplit` > 1), run by the four epilogue warps: this CTA's fp32
 // accumulator goes to the part's slot (float4 index (col / 4) * BM + row: a warp's stores of one
 // column group are contiguous); after a fence, one thread counts the part in.  The part counted last
 // (whichever CTA runs it) reads every part's slot in part order (ld.global.cg: from L2, written by
 // other SMs), adds them in that order, writes the tile as the unsplit epilogue would (store or
 // reduce-add) and resets the counter for the next launch.  No CTA waits for another, and the sum
-// is the same whichever part is last, so results stay bitwise reproducible.
+// is the same whichever part is last, so results stay bitwise reproducible.  The four warps meet on
+// two mbarriers (split_in, split_out; phase = nsplit & 1, the CTA's split parts so far) through the
+// engine's bounded wait, so a timeout elsewhere cannot leave a warp waiting.
 constexpr int kSplitMaxParts = 8;  // parts per tile at most (the host's kSplitMax)
 
 template <int CG>
 __device__ __forceinline__ void split_part(const GemmClass& c, SmemCtl* ctl, uint32_t taddr, int mt, int nt, int ks,
                                            int q, int warp, int lane, int orow, int ocol0, const CUtensorMap* out,
                                            uint32_t staging, uint8_t* stage_ptr, uint32_t& nstore, uint32_t tcount,
-                                           uint32_t rank, int32_t* status) {
+                                           uint32_t rank, uint32_t& nsplit, int32_t* status) {
   constexpr int kSlot = BM * BN / 4;  // float4 per partial tile
   if (mt >= c.n_mt) {                 // the empty half of an odd pair: no tile, no count
     epi_release<CG>(ctl, tcount, rank);
@@ -394,10 +392,18 @@ __device__ __forceinline__ void split_part(const GemmClass& c, SmemCtl* ctl, uin
   }
   epi_release<CG>(ctl, tcount, rank);
   __threadfence();
-  epi_bar_sync();
-  if (warp == 2 && lane == 0) ctl->split_last = atomicAdd(c.cnt + tile, 1) == c.ksplit - 1 ? 1 : 0;
-  epi_bar_sync();
-  if (!ctl->split_last) return;
+  __syncwarp();
+  const uint32_t par = nsplit & 1u;
+  ++nsplit;
+  if (lane == 0) mbar_arrive(&ctl->split_in);
+  if (warp == 2) {  // counts the part in once all four warps' rows are written
+    const bool in = wait_phase<CG>(ctl, &ctl->split_in, par, status);
+    if (lane == 0) {
+      ctl->split_last = in && atomicAdd(c.cnt + tile, 1) == c.ksplit - 1 ? 1 : 0;
+      mbar_arrive(&ctl->split_out);
+    }
+  }
+  if (!wait_phase<CG>(ctl, &ctl->split_out, par, status) || !ctl->split_last) return;
   __threadfence();
   if (orow < c.out_rows) {
 #pragma unroll 1
@@ -475,7 +481,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;
     uint8_t* stage_ptr = stg + (warp - 2) * STAGING_PER_WARP;
     const uint32_t staging = smem_u32(stage_ptr);
-    uint32_t tcount = 0, nstore = 0;
+    uint32_t tcount = 0, nstore = 0, nsplit = 0;
     for (uint32_t i = 0;; ++i) {
       const int u = feed_consume<CG>(feed, ctl, i, status, true, rank);
       if (u < 0) break;
@@ -512,7 +518,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!epi_acquire<CG>(ctl, tmem_base, tcount, warp, status, &taddr)) break;
       if (c.ksplit > 1) {
         split_part<CG>(c, ctl, taddr, mt, nt, ks, q, warp, lane, orow, ocol0, out, staging, stage_ptr, nstore, tcount,
-                       rank, status);
+                       rank, nsplit, status);
         ++tcount;
         continue;
       }
