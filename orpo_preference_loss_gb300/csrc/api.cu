@@ -205,18 +205,16 @@ int choose_nsplit(int64_t n_mt, int64_t n_vt, int sms) {
 }
 
 // Engine placement on the current device: 2-CTA clusters (slots = clusters) or single CTAs (slots =
-// SMs).  By default only the dh / dW GEMM (`gemm`) takes clusters: in the power-capped e4b step the
-// forward and the recompute ran faster on single CTAs and the GEMM on clusters.  ORPO_CTA_GROUP
-// forces one form; `allow_pair` false forces single CTAs (the backward skips' per-tile bitmaps and
-// lists), as does a device where no cluster fits.
+// SMs).  Every contraction takes clusters where they fit (measured faster for each of them);
+// ORPO_CTA_GROUP=1 forces single CTAs; `allow_pair` false forces them too (the backward skips'
+// per-tile bitmaps and lists).
 struct Placement {
   int cg;
   int slots;
 };
 
-Placement placement(int sms, bool gemm, bool allow_pair = true) {
-  const int force = engine_cta_group_override();
-  const bool want = allow_pair && (force == 2 || (force == 0 && gemm));
+Placement placement(int sms, bool allow_pair = true) {
+  const bool want = allow_pair && engine_cta_group_override() != 1;
   const int clusters = want ? engine_pair_clusters() : 0;
   return clusters > 0 ? Placement{2, clusters} : Placement{1, sms};
 }
@@ -348,7 +346,7 @@ int head_fwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   const int64_t nblocks = cdiv(V, vb);
   const int per_block = std::max<int>(1, nsplit_max / (int)nblocks);
   const bool side = q && q_side(M);
-  const Placement pl = placement(sms, false);
+  const Placement pl = placement(sms);
   const int64_t n_mu = cdiv(n_mt, pl.cg);  // M units: row tiles, or pairs of them
   L.cg = pl.cg;
   L.chunk = l2_chunk((int)n_mu, (int64_t)pl.cg * kBM * d * 2);
@@ -476,8 +474,7 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   bool split_zeroed = false;
   const int64_t sp = scratch_pitch(B);
   // the skips' bitmaps and tile lists are per 128-row tile
-  const Placement pr = placement(sms, false, !skip);  // recompute
-  const Placement pl = placement(sms, true, !skip);   // dh / dW GEMM
+  const Placement pl = placement(sms, !skip);  // recompute and dh / dW GEMM
   const uint32_t b_rows = kBN / pl.cg;                // rows or columns of the GEMMs' B per CTA
   const bool d64 = d % 64 == 0;  // MN-major h / W fetched with one 3-D box per stage
   RecLaunch R;
@@ -495,14 +492,14 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
   if (!dW) G.maps[5] = G.maps[4];
   // W maps over the whole bf16 head (encoded once), or per block over the dequantised copy
   auto encode_w = [&](const void* base, int64_t rows) {
-    return encode_map_2d(&R.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d, rows, d * 2, 64, kBN / pr.cg) &&
+    return encode_map_2d(&R.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d, rows, d * 2, 64, kBN / pl.cg) &&
            (d64 ? encode_map_mn3d(&G.maps[1], base, d, rows, d * 2, b_rows / 64)
                 : encode_map_2d(&G.maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, d, rows, d * 2, 64, 64));
   };
   if (!q && !encode_w(W, V)) return ORPO_ERR_CUDA;
   G.status = status;
   G.cg = pl.cg;
-  R.cg = pr.cg;
+  R.cg = pl.cg;
   R.targets = targets;
   R.mask = mask;
   R.lse = lse;
@@ -535,9 +532,9 @@ int head_bwd_impl(const void* h, const void* W, const QuantW* q, const int32_t* 
       R.w_row0 = q ? 0 : (int)v0;
       R.n_mt = n_mt;
       R.n_vt = n_vt;
-      const int64_t n_mu = cdiv(n_mt, pr.cg);
-      R.chunk = l2_chunk((int)n_mu, (int64_t)pr.cg * kBM * d * 2);
-      R.grid = (int)std::min<int64_t>(n_mu * n_vt, pr.slots) * pr.cg;
+      const int64_t n_mu = cdiv(n_mt, pl.cg);
+      R.chunk = l2_chunk((int)n_mu, (int64_t)pl.cg * kBM * d * 2);
+      R.grid = (int)std::min<int64_t>(n_mu * n_vt, pl.slots) * pl.cg;
       uint32_t *rowbits = nullptr, *colbits = nullptr;
       if (skip) {
         const int64_t slot = block % round_slots;
@@ -728,7 +725,7 @@ int orpo_debug_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N
   if (int e = device_check(&sms)) return e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   GemmLaunch G;
-  const Placement pl = placement(sms, true);
+  const Placement pl = placement(sms);
   const uint32_t b_rows = kBN / pl.cg;
   // MN-major operands whose contiguous extent is a multiple of 64 use the one-box 3-D fetch
   const int a_mode = a_mn_major ? (M % 64 == 0 ? 2 : 1) : 0;
@@ -845,7 +842,7 @@ extern "C" int orpo_head_fwd_static(const void* h, const void* W, const int32_t*
   FwdLaunch L;
   const int64_t n_mt = cdiv(M, kBM), n_vt = cdiv(V, kBN);
   const int64_t Mpad = n_mt * kBM;
-  const Placement pl = placement(sms, false);
+  const Placement pl = placement(sms);
   const int64_t n_mu = cdiv(n_mt, pl.cg);
   if (!encode_map_2d(&L.mh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, d, M, d * 2, 64, kBM) ||
       !encode_map_2d(&L.mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, d, V, d * 2, 64, kBN / pl.cg))

@@ -10,18 +10,22 @@
 // k-blocks (128-byte swizzle rows) of bf16 operands.
 //
 // Two forms, chosen by the template argument CG (the tcgen05 CTA group):
-//   CG = 1  one CTA per tile.  A stage holds A (128 x 64) and B (256 x 64): 48 KiB, 4 stages.
+//   CG = 1  one CTA per tile.  A stage holds one k-block of A (128 x 64) and B (256 x 64):
+//           48 KiB, 4 stages.
 //   CG = 2  a 2-CTA cluster computes a 256 x 256 tile with tcgen05.mma.cta_group::2, issued by
 //           the even CTA.  Each CTA fetches its own 128 rows of A and its own half (128 rows)
 //           of B into its own shared memory with plain (non-multicast) TMA loads, whose bytes
 //           are counted on the even CTA's `full` barrier; each CTA's tensor memory receives its
-//           128 rows of the accumulator.  A stage is 32 KiB, so 6 stages fit where 4 did, and
-//           every B tile crosses from L2 once per 256 rows instead of once per 128.  The even
-//           CTA's commits free the stages and publish the accumulators in both CTAs (two
+//           128 rows of the accumulator.  A k-block is 32 KiB per CTA, and a stage holds two
+//           (64 KiB, 3 stages): one wait and one pair of commits per 128 of K.  With one k-block
+//           per stage (six 32 KiB stages) the tensor pipe spent ~9% of its cycles on other
+//           work and the forward ran slower than on single CTAs; with two it is active ~90% of
+//           cycles.  Every B tile crosses from L2 once per 256 rows instead of once per 128.  The
+//           even CTA's commits free the stages and publish the accumulators in both CTAs (two
 //           unicast commits, one per CTA); the odd CTA's epilogue warps release accumulators
 //           and unit slots by remote arrivals on the even CTA's barriers.
 //
-// Operand staging in shared memory (per stage: A 16 KiB, B 32 KiB / CG):
+// Operand staging in shared memory (per k-block: A 16 KiB, B 32 KiB / CG):
 //   K-major operand  [rows, K] with K contiguous: one TMA box {64 (K), rows};
 //                    rows at 128 B pitch, 8-row swizzle atoms 1024 B apart (SBO).
 //   MN-major operand [K, rows] with rows contiguous: rows/64 TMA boxes {64, 64},
@@ -58,14 +62,18 @@ constexpr uint32_t STAGING_PER_WARP = 2 * BOX_BYTES;  // double-buffered
 constexpr uint32_t SMEM_CTL_BYTES = 256;
 
 // Shared-memory geometry of one CTA for CTA group CG.
+// A stage holds SUBS consecutive k-blocks, each laid out as a one-k-block stage would be: A
+// sub-blocks first, then B sub-blocks.  The 2-CTA form takes two per stage (one wait and one commit
+// pair per 128 of K), the single-CTA form one.
 template <int CG>
 struct Geo {
   static_assert(CG == 1 || CG == 2, "CTA group 1 or 2");
-  static constexpr int STAGES = CG == 2 ? 6 : 4;
-  static constexpr int B_ROWS = BN / CG;                // rows of the B tile this CTA fetches
-  static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;  // 32 KiB / CG
-  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr uint32_t TX_BYTES = CG * STAGE_BYTES;  // bytes one stage brings into the whole group
+  static constexpr int SUBS = CG == 2 ? 2 : 1;            // k-blocks per stage
+  static constexpr int STAGES = CG == 2 ? 3 : 4;
+  static constexpr int B_ROWS = BN / CG;                  // rows of the B tile this CTA fetches
+  static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;    // one k-block of B: 32 KiB / CG
+  static constexpr uint32_t SUB_BYTES = A_BYTES + B_BYTES;  // one k-block of A and B
+  static constexpr uint32_t STAGE_BYTES = SUBS * SUB_BYTES;
   static constexpr uint32_t STAGING_OFF = STAGES * STAGE_BYTES;
   static constexpr uint32_t CTL_OFF = STAGING_OFF + EPI_WARPS * STAGING_PER_WARP;
   static constexpr uint32_t SMEM = CTL_OFF + SMEM_CTL_BYTES + 1024;  // + slack to align the base to 1 KiB
@@ -338,7 +346,7 @@ __device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* sme
     for (int j = 0; ok && j < len; ++j) {
       const TileOps t = sched.tile(u, j);
       KWalk walk(t);
-      for (int i = 0; i < t.kblocks; ++i, ++it) {
+      for (int i = 0; i < t.kblocks; ++i, ++it) {  // one stage per pass: i advances by SUBS
         const int kb = walk.kblock(i);
         const uint32_t s = it % G::STAGES, ph = (it / G::STAGES) & 1u;
         if (!wait_phase<CG>(ctl, &ctl->empty[s], ph ^ 1u, status)) {
@@ -346,12 +354,17 @@ __device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* sme
           break;
         }
         uint8_t* a_dst = smem + s * G::STAGE_BYTES;
-        uint8_t* b_dst = a_dst + A_BYTES;
+        uint8_t* b_dst = a_dst + G::SUBS * A_BYTES;
+        const int nv = min(G::SUBS, t.kblocks - i);  // k-blocks in this stage
         // the even CTA's full barrier counts both CTAs' bytes; only the even CTA arrives on it
-        if (rank == 0) mbar_arrive_expect_tx(&ctl->full[s], G::TX_BYTES);
+        if (rank == 0) mbar_arrive_expect_tx(&ctl->full[s], (uint32_t)(nv * CG) * G::SUB_BYTES);
         const uint32_t bar = CG == 2 ? mapa_u32(smem_u32(&ctl->full[s]), 0) : smem_u32(&ctl->full[s]);
-        load_operand<CG>(t.a, bar, a_dst, BM, kb);
-        load_operand<CG>(t.b, bar, b_dst, G::B_ROWS, kb);
+        for (int j = 0; j < nv; ++j) {
+          const int kbj = j == 0 ? kb : walk.kblock(i + j);
+          load_operand<CG>(t.a, bar, a_dst + j * A_BYTES, BM, kbj);
+          load_operand<CG>(t.b, bar, b_dst + j * G::B_BYTES, G::B_ROWS, kbj);
+        }
+        i += nv - 1;
       }
     }
   }
@@ -397,23 +410,29 @@ __device__ void mma_role(const Sched& sched, const Feed& feed, uint8_t* smem, Sm
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
       const uint32_t idesc = make_idesc_bf16(BM * CG, BN, t.a.mn_major != 0, t.b.mn_major != 0);
-      for (int kb = 0; kb < t.kblocks; ++kb, ++it) {
+      for (int kb = 0; kb < t.kblocks; kb += G::SUBS, ++it) {
         const uint32_t s = it % G::STAGES, ph = (it / G::STAGES) & 1u;
         if (!wait_phase<CG>(ctl, &ctl->full[s], ph, status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t a_base = smem0 + s * G::STAGE_BYTES;
-        const uint32_t b_base = a_base + A_BYTES;
+        const int nv = min(G::SUBS, t.kblocks - kb);
 #pragma unroll
-        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-          const uint64_t ad = operand_desc(a_base, t.a.mn_major != 0, kk);
-          const uint64_t bd = operand_desc(b_base, t.b.mn_major != 0, kk);
-          if constexpr (CG == 2)
-            umma_bf16_cg2(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-          else
-            umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+        for (int j = 0; j < G::SUBS; ++j) {
+          if (j < nv) {
+            const uint32_t a_base = smem0 + s * G::STAGE_BYTES + j * A_BYTES;
+            const uint32_t b_base = smem0 + s * G::STAGE_BYTES + G::SUBS * A_BYTES + j * G::B_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              const uint64_t ad = operand_desc(a_base, t.a.mn_major != 0, kk);
+              const uint64_t bd = operand_desc(b_base, t.b.mn_major != 0, kk);
+              if constexpr (CG == 2)
+                umma_bf16_cg2(d_tmem, ad, bd, idesc, (kb | j | kk) != 0 ? 1u : 0u);
+              else
+                umma_bf16(d_tmem, ad, bd, idesc, (kb | j | kk) != 0 ? 1u : 0u);
+            }
+          }
         }
         commit_both<CG>(&ctl->empty[s]);  // frees the stage (in both CTAs) once these MMAs have read it
       }

@@ -291,8 +291,8 @@ int engine_pair_clusters() {
   return n > 0 ? n : 0;
 }
 
-// Read once per process: ORPO_CTA_GROUP=1 runs every engine kernel on single-CTA tiles, =2 every
-// one on 2-CTA clusters; otherwise only the dh / dW GEMM uses clusters.
+// Read once per process: ORPO_CTA_GROUP=1 runs every engine kernel on single-CTA tiles; otherwise
+// (unset, or =2) they run on 2-CTA clusters wherever clusters fit.
 int engine_cta_group_override() {
   static const int v = [] {
     const char* env = getenv("ORPO_CTA_GROUP");

@@ -50,9 +50,8 @@ __host__ __device__ inline int l2_chunk(int n_m, int64_t bytes_per_m) {
 
 // ---- tensor-core CTA group of the engine kernels (engine.cuh): 2 = 2-CTA clusters sharing each
 // tcgen05.mma, 1 = single-CTA tiles.  The host encodes the B operand's tensor map with boxes of
-// kBN / cg rows (each CTA of a pair fetches half of B).  By default the dh / dW GEMM runs on
-// clusters (where they fit) and the forward and the recompute on single CTAs, the faster choice
-// for each in the power-capped step; ORPO_CTA_GROUP=1 or =2 forces one form everywhere.
+// kBN / cg rows (each CTA of a pair fetches half of B).  Every contraction runs on clusters where
+// they fit; ORPO_CTA_GROUP=1 forces single CTAs everywhere.
 int engine_pair_clusters();       // co-resident 2-CTA clusters on the current device (0: none)
 int engine_cta_group_override();  // 0 (default policy), 1 or 2 (ORPO_CTA_GROUP)
 
