@@ -86,7 +86,10 @@ inline bool q_side(int64_t M) { return M >= kSideMinRows; }
 // copy would be all of W)
 BwdBlocks bwd_blocks(int64_t M, int64_t V, int64_t qd = 0) {
   const int64_t Mpad = std::max<int64_t>(kBM, cdiv(M, kBM) * kBM);
-  const int64_t Mc = std::min(Mpad, kMcMax);
+  // row blocks of equal height (a multiple of a 2-CTA pair's 256 rows) rather than full blocks and
+  // a short last one, whose launches would leave most SMs idle
+  const int64_t nmb = cdiv(Mpad, kMcMax);
+  const int64_t Mc = nmb == 1 ? Mpad : std::min(kMcMax, cdiv(cdiv(Mpad, nmb), 2 * kBM) * 2 * kBM);
   const int64_t Vpad = cdiv(V, kBN) * kBN;
   int64_t vc = (kScratchBudget / (2 * Mc)) / kBN * kBN;
   const int64_t wbuf = q_side(M) ? kWBudget / 2 : kWBudget;

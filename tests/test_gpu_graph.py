@@ -19,7 +19,7 @@ def outputs(head):
 
 @pytest.mark.parametrize("skip_eps", [0.0, 1e-5])
 def test_step_replays_in_a_cuda_graph(skip_eps):
-    w = workloads.make("e4b_sharp", M=16384 + 512, d=64, V=65536)   # 2 row blocks x 8 vocabulary blocks
+    w = workloads.make("e4b_sharp", M=16384 + 512, d=64, V=65536)   # 2 row blocks x 5 vocabulary blocks
     t = to_dev(w)
     h, W = t["h"].view(torch.bfloat16), t["W"].view(torch.bfloat16)
     head = orpo.OrpoHead(w.M, w.V, w.d, w.n_pairs, skip_eps=skip_eps)
