@@ -95,6 +95,9 @@ BwdBlocks bwd_blocks(int64_t M, int64_t V, int64_t qd = 0) {
   const int64_t wbuf = q_side(M) ? kWBudget / 2 : kWBudget;
   if (qd > 0) vc = std::min<int64_t>(vc, (wbuf / (2 * qd)) / kBN * kBN);
   vc = std::max<int64_t>(kBN, vc);
+  // vocabulary blocks of equal width too (multiples of 256 columns, never wider than the budget's)
+  const int64_t nvb = cdiv(Vpad, vc);
+  vc = cdiv(cdiv(Vpad, nvb), kBN) * kBN;
   return BwdBlocks{Mc, std::min(Vpad, vc)};
 }
 

@@ -106,11 +106,11 @@ def test_workspace_is_flat_in_M(lib):
     base = lib.orpo_head_workspace_bytes(16384, V, d)
     # dZ block (padded pitch) + GEMM unit counters + the backward skips' plan slots
     assert base <= (258 << 20) + (16 << 10) + (4 << 20) + 1024
-    # beyond one row block the blocks are balanced (equal heights), so the dZ block may be a little
-    # smaller, never larger
+    # blocks are balanced (equal heights and widths), so the dZ block may be a little smaller than
+    # at M = 16384, never larger
     for M in (16384, 20000, 65536, 131072, 16384 * 7 + 128):
         ws = lib.orpo_head_workspace_bytes(M, V, d)
-        assert base * 0.97 <= ws <= base
+        assert base * 0.9 <= ws <= base
     # far below any [M, V] buffer: 8192 x 262144 fp32 logits would be 8 GiB
     assert lib.orpo_head_workspace_bytes(8192, V, d) < (8192 * V * 4) // 16
     assert lib.orpo_head_workspace_bytes(-1, V, d) == 0

@@ -1,11 +1,12 @@
 """Dense-cotangent backward across several row and vocabulary blocks.
 
 The whole chain (forward, ORPO loss, backward) runs on the GPU through the C
-ABI, on a batch with two row blocks (M 19968 > 16384 rows per block) and seven
-vocabulary blocks with a ragged last one (V 50257, 8192 columns per block).
-The cotangent is the ORPO loss gradient itself, so every response row carries
-a nonzero g and every bf16 dZ block is dense: each dh tile is the reduce-add of
-seven vocabulary blocks and each dW tile of two row blocks.  The float64 oracle
+ABI, on a batch with two row blocks (M 19968 > 16384 rows per block: two of
+9984) and four vocabulary blocks with a ragged last one (V 50257: three of 12800
+columns and one of 11857).  The cotangent is the ORPO loss gradient itself, so
+every response row carries a nonzero g and every bf16 dZ block is dense: each dh
+tile is the reduce-add of four vocabulary blocks and each dW tile of two row
+blocks.  The float64 oracle
 runs the same chain on the same bf16 inputs ("Training — design" §2: the parity
 ladder against a plain reference, with a non-uniform cotangent).
 
@@ -59,7 +60,7 @@ def chain(request):
 def test_shape_spans_several_blocks(chain):
     w, _, _ = chain
     assert w.M > 16384 and w.M <= 2 * 16384          # two row blocks
-    assert 6 * 8192 < V < 7 * 8192                    # seven vocabulary blocks, the last ragged
+    assert 3 * 12800 < V < 4 * 12800                  # four vocabulary blocks, the last ragged
     assert np.all(w.mask == 1)                        # every row a response row: g dense
 
 
@@ -83,6 +84,6 @@ def test_dense_dW_every_block(chain):
     _, gpu, (_, _, _, _, dW) = chain
     assert relfro(gpu["dW"], dW) < GRAD_RELFRO
     assert np.max(np.abs(gpu["dW"] - dW)) <= 1e-2 * np.max(np.abs(dW))
-    for v0 in range(0, V, 8192):  # each vocabulary block on its own
-        blk = slice(v0, min(V, v0 + 8192))
+    for v0 in range(0, V, 12800):  # each vocabulary block on its own
+        blk = slice(v0, min(V, v0 + 12800))
         assert relfro(gpu["dW"][blk], dW[blk]) < GRAD_RELFRO, v0

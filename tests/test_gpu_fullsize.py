@@ -71,13 +71,13 @@ def test_backward_restricted_support(full):
 
 @pytest.mark.parametrize("d", [1600, 1544])
 def test_multiblock_ragged_vocab_and_hidden(d):
-    """M 20000 (two row blocks), V 50257 (seven vocabulary blocks, ragged tail); d 1544 is not a
-    multiple of 64, so the MN-major operands take the 2-D-box path."""
+    """M 20000 (two row blocks of 10240 rows), V 50257 (four vocabulary blocks of 12800 columns, the
+    last ragged); d 1544 is not a multiple of 64, so the MN-major operands take the 2-D-box path."""
     w = workloads.make("small", M=20000, d=d, V=50257)
     t = to_dev(w)
     W64 = f64(w.W)
     rng = np.random.default_rng(31)
-    rows = np.unique(np.concatenate([[0, w.M - 1, 16383, 16384], rng.choice(w.M, 36, replace=False)]))
+    rows = np.unique(np.concatenate([[0, w.M - 1, 10239, 10240], rng.choice(w.M, 36, replace=False)]))
     logp, lse, st = gpu_forward(t, w.M, w.V, w.d, 0.0)
     assert st == 0
     rl, rs = oracle.head_forward(f64(w.h[rows]), W64, w.targets[rows], w.mask[rows], 0.0)

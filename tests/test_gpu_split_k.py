@@ -1,12 +1,12 @@
 """Split K of the dh GEMM (few rows, long vocabulary blocks) against the oracle.
 
 With M 1024 the dh class has 8 row tiles of 128 rows (4 cluster units), each
-contracting over a vocabulary block of 131072 columns, so the kernel cuts every
-tile's K range into 8 parts that run on different SMs; the part that finishes
-last sums all parts in part order.  V 262151 makes three vocabulary blocks: the
-first split and stored, the second split and reduce-added onto it, the third (7
-columns, ragged) unsplit and reduce-added.  d 136 leaves most of each
-256-column tile outside the output.
+contracting over a vocabulary block of about 87k columns, so the kernel cuts every
+tile's K range into parts that run on different SMs; the part that finishes last
+sums all parts in part order.  V 262151 makes three vocabulary blocks of equal
+width (87552 columns, the last 87047): the first split and stored, the others
+split and reduce-added onto it.  d 136 leaves most of each 256-column tile
+outside the output.
 """
 
 import numpy as np
