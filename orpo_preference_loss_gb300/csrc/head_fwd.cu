@@ -228,16 +228,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // lse[t] = ln2 * (gM + log2 sum_k s_k 2^(m_k - gM));  logp[t] = z~[t,y_t] - lse[t] on response rows.
-__global__ void merge_kernel(const float* __restrict__ part_m, const float* __restrict__ part_s, int nsplit,
-                             int Mpad, int M, int V, const int32_t* __restrict__ targets,
-                             const uint8_t* __restrict__ mask, float* __restrict__ logp, float* __restrict__ lse,
-                             int32_t* status) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= M || !in_bounds(status, t, Mpad)) return;
+// A CTA takes 32 consecutive rows; warp g of its kMergeGroups warps reads the splits k = g, g + 8, ...
+// of those rows (one 128-byte line per split), so few rows still spread over many warps.  The
+// partial sums are added in group order, the same order on every run.
+constexpr int kMergeGroups = 8;
+__global__ void __launch_bounds__(32 * kMergeGroups)
+    merge_kernel(const float* __restrict__ part_m, const float* __restrict__ part_s, int nsplit, int Mpad, int M,
+                 int V, const int32_t* __restrict__ targets, const uint8_t* __restrict__ mask,
+                 float* __restrict__ logp, float* __restrict__ lse, int32_t* status) {
+  __shared__ float red_m[kMergeGroups][32];
+  __shared__ float red_s[kMergeGroups][32];
+  const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
+  const int t = blockIdx.x * 32 + lane;
+  const bool live = t < M && in_bounds(status, t, Mpad);
   float gm = -INFINITY;
-  for (int k = 0; k < nsplit; ++k) gm = fmaxf(gm, part_m[(size_t)k * Mpad + t]);
+  if (live)
+    for (int k = grp; k < nsplit; k += kMergeGroups) gm = fmaxf(gm, part_m[(size_t)k * Mpad + t]);
+  red_m[grp][lane] = gm;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kMergeGroups; ++j) gm = fmaxf(gm, red_m[j][lane]);
   float S = 0.f;
-  for (int k = 0; k < nsplit; ++k) S += part_s[(size_t)k * Mpad + t] * exp2f(part_m[(size_t)k * Mpad + t] - gm);
+  if (live)
+    for (int k = grp; k < nsplit; k += kMergeGroups)
+      S += part_s[(size_t)k * Mpad + t] * exp2f(part_m[(size_t)k * Mpad + t] - gm);
+  red_s[grp][lane] = S;
+  __syncthreads();
+  if (grp != 0 || !live) return;
+  S = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMergeGroups; ++j) S += red_s[j][lane];
   const float l = (gm + log2f(S)) * kLn2;
   lse[t] = l;
   int32_t err = 0;
@@ -307,10 +327,9 @@ cudaError_t launch_forward_logits(const FwdLaunch& L, cudaStream_t st) {
 }
 
 cudaError_t launch_forward_merge(const FwdLaunch& L, int nsplit_total, cudaStream_t st) {
-  const int threads = 256;
   prof_begin(K_MERGE, st);
-  merge_kernel<<<(L.M + threads - 1) / threads, threads, 0, st>>>(L.part_m, L.part_s, nsplit_total, L.Mpad, L.M, L.V,
-                                                                  L.targets, L.mask, L.logp, L.lse, L.status);
+  merge_kernel<<<(L.M + 31) / 32, 32 * kMergeGroups, 0, st>>>(L.part_m, L.part_s, nsplit_total, L.Mpad, L.M, L.V,
+                                                              L.targets, L.mask, L.logp, L.lse, L.status);
   prof_end(K_MERGE, st);
   return cudaGetLastError();
 }
