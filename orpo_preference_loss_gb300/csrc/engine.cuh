@@ -65,13 +65,20 @@ constexpr uint32_t SMEM_CTL_BYTES = 256;
 // A stage holds SUBS consecutive k-blocks, each laid out as a one-k-block stage would be: A
 // sub-blocks first, then B sub-blocks.  The 2-CTA form takes two per stage (one wait and one commit
 // pair per 128 of K), the single-CTA form one.
-template <int CG>
+// W (wide, 2-CTA only): the pair's tile is 256 x 512, two 256-column halves that share the A tile.
+// Each CTA fetches 128 rows of each half of B (32 KiB per k-block, one k-block per stage, four
+// stages), and the single accumulator takes all 512 TMEM columns: the epilogue no longer overlaps
+// the next tile's MMAs, but each k-block moves a quarter fewer operand bytes per flop.
+template <int CG, bool W = false>
 struct Geo {
   static_assert(CG == 1 || CG == 2, "CTA group 1 or 2");
-  static constexpr int SUBS = CG == 2 ? 2 : 1;            // k-blocks per stage
-  static constexpr int STAGES = CG == 2 ? 3 : 4;
-  static constexpr int B_ROWS = BN / CG;                  // rows of the B tile this CTA fetches
-  static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;    // one k-block of B: 32 KiB / CG
+  static_assert(!W || CG == 2, "wide tiles run on 2-CTA clusters");
+  static constexpr int SUBS = W ? 1 : (CG == 2 ? 2 : 1);  // k-blocks per stage
+  static constexpr int STAGES = W ? 4 : (CG == 2 ? 3 : 4);
+  static constexpr int B_ROWS = (W ? 2 : 1) * BN / CG;    // rows of B this CTA fetches per k-block
+  static constexpr int TN = W ? 2 * BN : BN;              // output columns of a tile
+  static constexpr int NACC = W ? 1 : 2;                  // accumulators in TMEM
+  static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;    // one k-block of B: 32 KiB / CG (wide: 32 KiB)
   static constexpr uint32_t SUB_BYTES = A_BYTES + B_BYTES;  // one k-block of A and B
   static constexpr uint32_t STAGE_BYTES = SUBS * SUB_BYTES;
   static constexpr uint32_t STAGING_OFF = STAGES * STAGE_BYTES;
@@ -330,10 +337,10 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, in
 }
 
 // ---------------------------------------------------------------- producer (one thread per CTA)
-template <int CG, class Sched>
+template <int CG, bool W, class Sched>
 __device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* smem, SmemCtl* ctl, int32_t* status,
                               uint32_t rank) {
-  using G = Geo<CG>;
+  using G = Geo<CG, W>;
   uint32_t it = 0;
   bool ok = true;
   for (uint32_t i = 0; ok; ++i) {
@@ -362,7 +369,14 @@ __device__ void producer_role(const Sched& sched, const Feed& feed, uint8_t* sme
         for (int j = 0; j < nv; ++j) {
           const int kbj = j == 0 ? kb : walk.kblock(i + j);
           load_operand<CG>(t.a, bar, a_dst + j * A_BYTES, BM, kbj);
-          load_operand<CG>(t.b, bar, b_dst + j * G::B_BYTES, G::B_ROWS, kbj);
+          if constexpr (W) {  // the two halves of the wide tile: B rows mn0 and mn0 + BN
+            Operand b2 = t.b;
+            b2.mn0 += BN;
+            load_operand<CG>(t.b, bar, b_dst + j * G::B_BYTES, BN / CG, kbj);
+            load_operand<CG>(b2, bar, b_dst + j * G::B_BYTES + G::B_BYTES / 2, BN / CG, kbj);
+          } else {
+            load_operand<CG>(t.b, bar, b_dst + j * G::B_BYTES, G::B_ROWS, kbj);
+          }
         }
         i += nv - 1;
       }
@@ -387,10 +401,10 @@ __device__ __forceinline__ void commit_both(uint64_t* bar) {
   }
 }
 
-template <int CG, class Sched>
+template <int CG, bool W, class Sched>
 __device__ void mma_role(const Sched& sched, const Feed& feed, uint8_t* smem, SmemCtl* ctl, uint32_t tmem_base,
                          int32_t* status) {
-  using G = Geo<CG>;
+  using G = Geo<CG, W>;
   uint32_t it = 0, tcount = 0;
   bool ok = true;
   const uint32_t smem0 = smem_u32(smem);
@@ -401,7 +415,7 @@ __device__ void mma_role(const Sched& sched, const Feed& feed, uint8_t* smem, Sm
     for (int j = 0; ok && j < len; ++j) {
       const TileOps t = sched.tile(u, j);
       if (t.kblocks == 0) continue;  // empty tile: no accumulator (the epilogue knows)
-      const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
+      const uint32_t buf = G::NACC == 2 ? tcount & 1u : 0u, aph = G::NACC == 2 ? (tcount >> 1) & 1u : tcount & 1u;
       ++tcount;
       if (!wait_phase<CG>(ctl, &ctl->acc_empty[buf], aph ^ 1u, status)) {
         ok = false;
@@ -431,6 +445,9 @@ __device__ void mma_role(const Sched& sched, const Feed& feed, uint8_t* smem, Sm
                 umma_bf16_cg2(d_tmem, ad, bd, idesc, (kb | j | kk) != 0 ? 1u : 0u);
               else
                 umma_bf16(d_tmem, ad, bd, idesc, (kb | j | kk) != 0 ? 1u : 0u);
+              if constexpr (W)  // the second half: B rows BN on, accumulator columns BN on
+                umma_bf16_cg2(d_tmem + BN, ad, operand_desc(b_base + G::B_BYTES / 2, t.b.mn_major != 0, kk), idesc,
+                              (kb | j | kk) != 0 ? 1u : 0u);
             }
           }
         }
@@ -452,10 +469,10 @@ __device__ void mma_role(const Sched& sched, const Feed& feed, uint8_t* smem, Sm
 
 // Waits until accumulator tile `tcount` is ready; returns its TMEM address for
 // this warp's 32 lanes (column 0 of the tile).
-template <int CG = 1>
+template <int CG = 1, bool W = false>
 __device__ __forceinline__ bool epi_acquire(SmemCtl* ctl, uint32_t tmem_base, uint32_t tcount, int warp,
                                             int32_t* status, uint32_t* taddr) {
-  const uint32_t buf = tcount & 1u, aph = (tcount >> 1) & 1u;
+  const uint32_t buf = W ? 0u : tcount & 1u, aph = W ? tcount & 1u : (tcount >> 1) & 1u;
   if (!wait_phase<CG>(ctl, &ctl->acc_full[buf], aph, status)) return false;
   tc_fence_after();
   *taddr = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + buf * BN;
@@ -463,11 +480,11 @@ __device__ __forceinline__ bool epi_acquire(SmemCtl* ctl, uint32_t tmem_base, ui
 }
 
 // The accumulator's counter lives in the even CTA: the odd CTA's warps arrive on it remotely.
-template <int CG = 1>
+template <int CG = 1, bool W = false>
 __device__ __forceinline__ void epi_release(SmemCtl* ctl, uint32_t tcount, uint32_t rank = 0) {
   tc_fence_before();
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) arrive_leader<CG>(&ctl->acc_empty[tcount & 1u], rank);
+  if ((threadIdx.x & 31) == 0) arrive_leader<CG>(&ctl->acc_empty[W ? 0u : tcount & 1u], rank);
 }
 
 // 32 fp32 values of one row -> 128-byte swizzled row `lane` of a 32 x 128 B staging box
@@ -495,10 +512,10 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t box, int lane, const uin
 // which walks the units with feed_consume<CG>(feed, ctl, i, status, true, rank); `side()` is the
 // spare warps' job, independent of the pipeline (it touches no barrier, TMEM or staging box).
 // CG = 2 must run in 2-CTA clusters.
-template <int CG, class Sched, class EpiFn, class SideFn>
+template <int CG, bool W = false, class Sched, class EpiFn, class SideFn>
 __device__ __forceinline__ void run_cta(const Sched& sched, const Feed& feed, int32_t* status, EpiFn&& epilogue,
                                         SideFn&& side) {
-  using G = Geo<CG>;
+  using G = Geo<CG, W>;
   uint8_t* smem = smem_base_aligned();
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + G::CTL_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -534,9 +551,9 @@ __device__ __forceinline__ void run_cta(const Sched& sched, const Feed& feed, in
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer_role<CG>(sched, feed, smem, ctl, status, rank);
+    if (lane == 0) producer_role<CG, W>(sched, feed, smem, ctl, status, rank);
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_role<CG>(sched, feed, smem, ctl, tmem_base, status);
+    if (lane == 0 && rank == 0) mma_role<CG, W>(sched, feed, smem, ctl, tmem_base, status);
   } else if (warp < SIDE_WARP) {
     epilogue(smem + G::STAGING_OFF, ctl, tmem_base, warp, lane, rank);
   } else {

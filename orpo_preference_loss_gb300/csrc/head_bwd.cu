@@ -274,8 +274,9 @@ struct GemmClass {
 
 // Unit = (class, M unit, N tile); an M unit is one 128-row output tile (CG = 1) or a pair's two
 // (CG = 2: CTA rank r takes output tile 2m + r and fetches half of the B tile).
-template <int CG>
+template <int CG, bool W = false>
 struct GemmSched {
+  static constexpr int TN = Geo<CG, W>::TN;  // output columns of a tile (512 for the wide form)
   const CUtensorMap* maps[6];
   GemmClass cls[2];
   int32_t* status;
@@ -333,7 +334,7 @@ struct GemmSched {
     const int kb0 = kb_first(c, ks);
     TileOps t;
     t.a = Operand{map(c.a_map), c.a_mn, c.a_mn_base + mt * BM, c.a_k_base + kb0 * BK};
-    t.b = Operand{map(c.b_map), c.b_mn, c.b_mn_base + nt * BN + rank * (BN / CG), c.b_k_base + kb0 * BK};
+    t.b = Operand{map(c.b_map), c.b_mn, c.b_mn_base + nt * TN + rank * (BN / CG), c.b_k_base + kb0 * BK};
     t.kblocks = kb_first(c, ks + 1) - kb0;
     if (CG == 1 && c.kbits != nullptr) {
       const int br = in_bounds(status, mt >> c.list_shift, c.kbits_rows) ? mt >> c.list_shift : 0;
@@ -458,12 +459,13 @@ __device__ __forceinline__ void split_part(const GemmClass& c, SmemCtl* ctl, uin
   if (warp == 2 && lane == 0) c.cnt[tile] = 0;
 }
 
-template <int CG>
+template <int CG, bool W>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
                 const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
-                const __grid_constant__ CUtensorMap m4, const __grid_constant__ CUtensorMap m5, GemmSched<CG> sched,
-                int* counter, int32_t* status) {
+                const __grid_constant__ CUtensorMap m4, const __grid_constant__ CUtensorMap m5,
+                GemmSched<CG, W> sched, int* counter, int32_t* status) {
+  constexpr int TN = GemmSched<CG, W>::TN;
   sched.maps[0] = &m0;
   sched.maps[1] = &m1;
   sched.maps[2] = &m2;
@@ -476,8 +478,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int i = 0; i < 6; ++i) tma_prefetch_desc(sched.maps[i]);
   }
   const Feed feed{counter, sched.num_units()};
-  run_cta<CG>(sched, feed, status, [&](uint8_t* stg, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane,
-                                       uint32_t rank) {
+  run_cta<CG, W>(sched, feed, status, [&](uint8_t* stg, SmemCtl* ctl, uint32_t tmem_base, int warp, int lane,
+                                          uint32_t rank) {
     const int q = warp & 3;
     uint8_t* stage_ptr = stg + (warp - 2) * STAGING_PER_WARP;
     const uint32_t staging = smem_u32(stage_ptr);
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const GemmClass c = sched.pick(k);
       const CUtensorMap* out = sched.map(c.out_map);
       const int orow = c.out_row_base + mt * BM + 32 * q;
-      const int ocol0 = c.out_col_base + nt * BN;
+      const int ocol0 = c.out_col_base + nt * TN;
       if (CG == 1 && sched.tile(u, 0).kblocks == 0) {
         // empty sparse tile: nothing to add; a first (store) write still owes the tile its zeros
         if (!c.reduce && orow < c.out_rows) {
@@ -515,25 +517,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         continue;
       }
       uint32_t taddr;
-      if (!epi_acquire<CG>(ctl, tmem_base, tcount, warp, status, &taddr)) break;
-      if (c.ksplit > 1) {
-        split_part<CG>(c, ctl, taddr, mt, nt, ks, q, warp, lane, orow, ocol0, out, staging, stage_ptr, nstore, tcount,
-                       rank, nsplit, status);
-        ++tcount;
-        continue;
+      if (!epi_acquire<CG, W>(ctl, tmem_base, tcount, warp, status, &taddr)) break;
+      if constexpr (!W) {  // (the host never splits K with wide tiles)
+        if (c.ksplit > 1) {
+          split_part<CG>(c, ctl, taddr, mt, nt, ks, q, warp, lane, orow, ocol0, out, staging, stage_ptr, nstore,
+                         tcount, rank, nsplit, status);
+          ++tcount;
+          continue;
+        }
       }
       if (mt < c.n_mt && orow < c.out_rows) {  // (the empty half of an odd pair stores nothing)
         uint32_t ra[32], rb[32];
         tmem_ld32(taddr, ra);
 #pragma unroll 1
-        for (int ch = 0; ch < BN / 32; ch += 2) {
+        for (int ch = 0; ch < TN / 32; ch += 2) {
           tmem_ld_wait(ra);
           tmem_ld32(taddr + (ch + 1) * 32, rb);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             if (h == 1) {
               tmem_ld_wait(rb);
-              if (ch + 2 < BN / 32) tmem_ld32(taddr + (ch + 2) * 32, ra);
+              if (ch + 2 < TN / 32) tmem_ld32(taddr + (ch + 2) * 32, ra);
             }
             const int col = ocol0 + (ch + h) * 32;
             if (col < c.out_cols) {
@@ -559,7 +563,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      epi_release<CG>(ctl, tcount, rank);
+      epi_release<CG, W>(ctl, tcount, rank);
       ++tcount;
     }
     if (lane == 0) bulk_wait_group<0>();
@@ -594,11 +598,11 @@ cudaError_t launch_rec_cap(const RecLaunch& L, cudaStream_t st) {
                              : launch_rec_kernel<kCapOff, kFilter, CG>(L, st);
 }
 
-template <int CG>
+template <int CG, bool W>
 cudaError_t launch_gemm_cg(const GemmLaunch& L, cudaStream_t st, int kind) {
   static std::atomic<int> smem_set[64];
-  if (cudaError_t e = opt_in_smem(gemm_kernel<CG>, Geo<CG>::SMEM, smem_set)) return e;
-  GemmSched<CG> sched;
+  if (cudaError_t e = opt_in_smem(gemm_kernel<CG, W>, Geo<CG, W>::SMEM, smem_set)) return e;
+  GemmSched<CG, W> sched;
   for (int i = 0; i < 6; ++i) sched.maps[i] = nullptr;
   sched.status = nullptr;
   for (int k = 0; k < 2; ++k) {
@@ -610,8 +614,8 @@ cudaError_t launch_gemm_cg(const GemmLaunch& L, cudaStream_t st, int kind) {
                              h.kbits_rows, h.ksplit,   h.part,       h.cnt};
   }
   prof_begin(kind, st);
-  const cudaError_t e = launch_engine(gemm_kernel<CG>, CG, L.grid, Geo<CG>::SMEM, st, L.maps[0], L.maps[1], L.maps[2],
-                                      L.maps[3], L.maps[4], L.maps[5], sched, L.counter, L.status);
+  const cudaError_t e = launch_engine(gemm_kernel<CG, W>, CG, L.grid, Geo<CG, W>::SMEM, st, L.maps[0], L.maps[1],
+                                      L.maps[2], L.maps[3], L.maps[4], L.maps[5], sched, L.counter, L.status);
   prof_end(kind, st);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -623,7 +627,8 @@ cudaError_t launch_recompute(const RecLaunch& L, cudaStream_t st) {
 }
 
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind) {
-  return L.cg == 2 ? launch_gemm_cg<2>(L, st, kind) : launch_gemm_cg<1>(L, st, kind);
+  if (L.cg == 2) return L.wide ? launch_gemm_cg<2, true>(L, st, kind) : launch_gemm_cg<2, false>(L, st, kind);
+  return launch_gemm_cg<1, false>(L, st, kind);
 }
 
 }  // namespace orpo

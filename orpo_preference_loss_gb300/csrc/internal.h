@@ -174,6 +174,7 @@ struct GemmLaunch {
   int32_t* status;
   int grid;
   int cg = 1;    // CTA group (1 whenever a class has sparse K)
+  int wide = 0;  // 2-CTA only, no split K: 256 x 512 tiles (classes' n_nt count 512-column tiles)
 };
 cudaError_t launch_gemm(const GemmLaunch& L, cudaStream_t st, int kind);
 
