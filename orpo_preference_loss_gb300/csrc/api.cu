@@ -170,8 +170,9 @@ size_t split_bytes(int64_t M, int64_t d, int64_t qd = 0) {
 // Wide (256 x 512) GEMM tiles: a quarter fewer operand bytes per flop, but the accumulator takes all of
 // TMEM, so a tile's epilogue no longer overlaps the next tile's MMAs, and twice-as-long tiles make the
 // last wave coarser.  Measured 6-10% faster per tile on wave-aligned shapes.  Taken on 2-CTA clusters
-// without split K when the output width is a multiple of 512 columns and there are at least three
-// waves of wide tiles.  ORPO_GEMM_WIDE=0 never takes them, =1 wherever they are legal.
+// without split K when padding the output width to 512 columns adds at most an eighth (d 3840 pads to
+// 4096 and still gains 2%) and there are at least three waves of wide tiles.  ORPO_GEMM_WIDE=0 never
+// takes them, =1 wherever they are legal.
 int gemm_wide_override() {
   static const int v = [] {
     const char* e = getenv("ORPO_GEMM_WIDE");
@@ -184,7 +185,7 @@ bool use_wide(int cg, int ksplit, int64_t out_cols, int64_t wide_units, int slot
   if (cg != 2 || ksplit > 1) return false;
   const int o = gemm_wide_override();
   if (o >= 0) return o == 1;
-  return out_cols % (2 * kBN) == 0 && wide_units >= 3 * (int64_t)slots;
+  return cdiv(out_cols, 2 * kBN) * 2 * kBN * 8 <= out_cols * 9 && wide_units >= 3 * (int64_t)slots;
 }
 
 int choose_ksplit(int64_t units, int64_t kblocks, int64_t tiles, int slots, size_t part_bytes, int64_t other_kb) {
