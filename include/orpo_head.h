@@ -297,7 +297,10 @@ const char* orpo_status_string(int code);
  * stored transposed as [K, M] (a_mn_major = 1); B is [N, K] (b_mn_major = 0)
  * or stored as [K, N] (b_mn_major = 1); C is fp32 [M, N] row-major and is
  * overwritten.  M, N, K >= 1; the contiguous extent of every operand must be a
- * multiple of 8 elements and of C a multiple of 4.
+ * multiple of 8 elements and of C a multiple of 4.  It takes the engine's tile
+ * forms by the same rules as the head's dh / dW contraction (2-CTA clusters where
+ * they fit, 256 x 512 pair tiles for wide outputs with several waves of tiles),
+ * including the ORPO_CTA_GROUP and ORPO_GEMM_WIDE overrides.
  */
 int orpo_debug_gemm(const void* A_bf16, const void* B_bf16, float* C, int64_t M, int64_t N,
                     int64_t K, int a_mn_major, int b_mn_major, int32_t* status, void* stream);
